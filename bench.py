@@ -1,0 +1,380 @@
+"""Throughput of the fused LM-head forward + backward on GB300.
+
+One step = the whole scoring path on one batch of synthetic inputs:
+keep mask from the loss mask (next-token shift) -> compaction -> chunked
+tcgen05 projection with the online-softmax epilogue -> split-V merge ->
+expansion; then the backward: compaction, logit recomputation with the dZ
+epilogue, dHidden (scattered back) and dW contractions per chunk.
+
+Default workload: 30B-MoE-shaped RL head, N=65536 packed tokens, H=4096,
+V=151936, bf16, sequences of length ~U[512, 8192] with a prompt fraction
+~U[0.3, 0.7] masked (about half the rows kept), differentiable entropy
+(grad_entropy = -0.01).
+
+Prints one JSON line.  `--impl reference` times the float64 CPU oracle on a
+bounded sample of kept rows of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused LM-head fwd+bwd kept-tokens/s and TFLOP/s (% of GB300 bf16 tensor peak)"
+UNIT = "kept-tokens/s"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d["bf16_tflops_sustained"], d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _oracle_sample(inp, keep, rows, want_grad=True):
+    """Float64 oracle on `rows` kept rows (full forward + backward work)."""
+    import numpy as np
+    from oracle import lmhead_oracle as O
+    idx = np.flatnonzero(keep)
+    pick = idx[np.linspace(0, len(idx) - 1, rows).astype(np.int64)]
+    h = inp["hidden"][pick].float().cpu().double().numpy()
+    y = inp["targets"][pick].cpu().numpy()
+    g1 = inp["grad_logprob"][pick].cpu().double().numpy()
+    g2 = (inp["grad_entropy"][pick].cpu().double().numpy()
+          if inp["grad_entropy"] is not None else None)
+    return h, y, g1, g2
+
+
+def cpu_oracle_rate(inp, keep_np, W64, rows):
+    from oracle import lmhead_oracle as O
+    h, y, g1, g2 = _oracle_sample(inp, keep_np, rows)
+    t0 = time.perf_counter()
+    O.score_rows(h, W64, y, g1, g2)
+    dt = time.perf_counter() - t0
+    return rows / dt, dt
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """Reference arm: the float64 CPU oracle, timed on host cores."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    from oracle import lmhead_oracle as O
+    from sft_keep_mask_gb300 import synth
+    w = synth.workload(args.workload)
+    inp = synth.make_inputs(w, device="cpu")
+    keep = O.build_keep_mask([c.numpy() for c in inp["components"]], inp["seq_lens"]) \
+        if "components" in inp else inp["keep"].numpy()
+    nk = int(keep.sum())
+    W64 = inp["weight"].float().double().numpy()
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        cpu_oracle_rate(inp, keep, W64, rows)
+    times = []
+    for _ in range(args.steps):
+        _, dt = cpu_oracle_rate(inp, keep, W64, rows)
+        times.append(dt)
+    tot = sum(times)
+    value = rows * args.steps / tot
+    flops = 8.0 * rows * w.H * w.V * args.steps
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "N": w.N, "H": w.H, "V": w.V, "kept_rows": nk,
+                   "sample_rows_per_step": rows},
+        "tflops": flops / tot / 1e12,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                         "sample": f"{rows} kept rows per step, full H and V, forward + "
+                                   "dhidden + dW contribution, float64 numpy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    from sft_keep_mask_gb300 import lmhead as L
+    from sft_keep_mask_gb300 import synth
+    from sft_keep_mask_gb300.api import LMHeadScorer
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L.lib()
+
+    w = synth.workload(args.workload)
+    w = synth.workload(args.workload, seed=w.seed + 100 * rank)
+    inp = synth.make_inputs(w, device=dev)
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=args.chunk_rows, device=dev)
+    comps = inp.get("components")
+    lens = inp.get("seq_lens")
+    offsets = None
+    if comps is not None:
+        off = np.zeros(len(lens) + 1, np.int32)
+        off[1:] = np.cumsum(lens)
+        offsets = torch.from_numpy(off).to(dev)
+    N, H, V = w.N, w.H, w.V
+    keep = torch.empty(N, dtype=torch.uint8, device=dev)
+    lp = torch.empty(N, dtype=torch.float32, device=dev)
+    ent = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws = sc.workspace
+    g_ent = inp["grad_entropy"] if args.entropy_grad else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step(hidden, targets, loss_mask, offs, g_lp, g_e):
+        if loss_mask is not None:
+            L.lmhead_build_keep_mask(loss_mask, None, None, offs, keep, stream)
+        else:
+            keep.copy_(inp["keep"])
+        L.lmhead_fwd(hidden, inp["weight"], targets, keep, True, lp, ent, lse, ws,
+                     args.chunk_rows, stream)
+        L.lmhead_bwd(hidden, inp["weight"], targets, keep, lse, ent, g_lp, g_e, dh, dW, False,
+                     ws, args.chunk_rows, stream)
+
+    loss_mask = comps[0] if comps is not None else None
+    dev_args = (inp["hidden"], inp["targets"], loss_mask, offsets, inp["grad_logprob"], g_ent)
+    for _ in range(args.warmup):
+        step(*dev_args)
+    torch.cuda.synchronize(dev)
+    status = L.lmhead_get_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    nk = int(keep.sum().item())
+
+    # ---------------------------------------------------------- device-timed
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    L.lmhead_profile_enable(True)
+    L.lmhead_profile_read()
+    launches0 = L.lmhead_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(*dev_args)
+        ev1.record(stream)
+        barrier()
+    L.lmhead_profile_enable(False)
+    launches = L.lmhead_launch_count() - launches0
+    prof = L.lmhead_profile_read()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms, float(nk)], device=dev, dtype=torch.float64)
+        mx = t.clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        sm = t.clone()
+        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
+        ms_max, nk_total = float(mx[0]), float(sm[1])
+    else:
+        ms_max, nk_total = ms, float(nk)
+    sec = ms_max / 1e3
+    value = nk_total * args.steps / sec
+    flops_step = 8.0 * nk_total * H * V
+    tflops = flops_step * args.steps / sec / 1e12
+    burst, sustained, hbm, peak_src = _peaks()
+
+    # dominant kernel of the step (largest summed device time)
+    kinds = {k: v for k, v in prof.items() if v[0] > 0}
+    tot_ms = sum(v[1] for v in kinds.values()) or 1.0
+    gemm_flops = {"gemm_fwd": 2.0, "gemm_dz": 2.0, "gemm_dh": 2.0, "gemm_dw": 2.0}
+    dom = max(kinds, key=lambda k: kinds[k][1])
+    dom_ms = kinds[dom][1]
+    if dom in gemm_flops:
+        alg = gemm_flops[dom] * nk * H * V * args.steps  # flops of this kernel in the region
+        achieved = alg / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": sustained,
+                "unit": "TFLOP/s", "frac": achieved / sustained,
+                "frac_of_burst_peak": achieved / burst, "peak_source": f"{peak_src} sustained",
+                "traffic": None}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": hbm, "unit": "GB/s",
+                "frac": None, "traffic": None}
+    kernels = {k: {"launches": v[0], "ms": v[1], "share": v[1] / tot_ms} for k, v in kinds.items()}
+    gemm_ms = sum(kinds[k][1] for k in gemm_flops if k in kinds)
+    gemm_tflops = 8.0 * nk * H * V * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms else None
+
+    # ---------------------------------------------------------- end to end
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory() if t is not None else None  # noqa: E731
+        host = [pin(inp["hidden"]), pin(inp["targets"]), pin(loss_mask), pin(offsets),
+                pin(inp["grad_logprob"]), pin(g_ent)]
+        dbuf = [torch.empty_like(t, device=dev) if t is not None else None for t in host]
+        out_lp = torch.empty(N, dtype=torch.float32).pin_memory()
+        out_ent = torch.empty(N, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
+        d2h = 2 * N * 4
+
+        def e2e_step():
+            for d, hst in zip(dbuf, host):
+                if d is not None:
+                    d.copy_(hst, non_blocking=True)
+            step(*dbuf)
+            out_lp.copy_(lp, non_blocking=True)
+            out_ent.copy_(ent, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        barrier()
+        el = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([el], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            el = float(t[0])
+        e2e = {"value": nk_total * args.steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * el / args.steps}
+
+    # ---------------------------------------------------------- CPU oracle
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        keep_np = keep.cpu().numpy()
+        W64 = inp["weight"].float().cpu().double().numpy()
+        rate, dt = cpu_oracle_rate(inp, keep_np, W64, args.ref_rows)
+        cpu = {"value": rate, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+               "sample": f"{args.ref_rows} kept rows, full H and V: forward + dhidden + dW "
+                         f"contribution in float64 numpy ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "N": N, "H": H, "V": V, "kept_rows": nk,
+                       "kept_frac": nk / N, "chunk_rows": args.chunk_rows or 8192,
+                       "entropy": "differentiable" if args.entropy_grad else "metric-only",
+                       "l2": "inputs larger than L2 (W 1.2 GB, hidden 0.5 GB)",
+                       "parallelism": f"replicas x{world}"},
+            "tflops": tflops, "frac_of_peak": tflops / burst,
+            "frac_of_sustained_peak": tflops / sustained,
+            "gemm_tflops": gemm_tflops,
+            "roofline": roof, "kernels": kernels, "gpu_launches": launches,
+            "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="moe30b_rl")
+    ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--entropy-grad", type=int, default=1)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * lmhead.h -- C ABI of the GB300 (sm_103a) fused LM-head scoring library.
+ *
+ * What it computes, for hidden states h[N,H] and an LM-head weight W[V,H]
+ * (bf16, row-major), targets y[N] and a keep mask keep[N]:
+ *
+ *   for every kept row i (keep[i] != 0), with z = h[i] W^T (never stored):
+ *     lse[i]      = log sum_v exp(z_v)
+ *     logprob[i]  = z_{y[i]} - lse[i]
+ *     entropy[i]  = -sum_v p_v log p_v,       p = softmax(z)
+ *   and for a gradient g_lp[i] on logprob and g_ent[i] on entropy:
+ *     dz_v        = g_lp (1[v = y] - p_v) - g_ent p_v (log p_v + entropy)
+ *     dhidden[i]  = dz W            dW += dz^T h[i]
+ *   skipped rows get logprob = entropy = lse = 0, dhidden = 0, and add
+ *   nothing to dW.
+ *
+ * Sources (cited by page title and section):
+ *   [P1] prime-rl pull request #3326, "Don't compute the logprobs and their
+ *        gradients for tokens no loss component reads": maintainer comment
+ *        (the FLOPs are in the [N,H] x [H,V] vocab matmul) and "Overview"
+ *        (keep mask = union of RL loss mask, CE weights and ref-KL weights
+ *        after the next-token shift; compact -> chunked logprob/entropy ->
+ *        expand with zeros; token chunk 8192).
+ *   [P2] SkyRL pull request #2374, "feat(megatron): fuse LM-head entropy for
+ *        RL": "How it works" (one projection gives log-prob and entropy;
+ *        metric-only entropy adds no gradient work; entropy-loss mode keeps
+ *        the entropy derivative) and the gemini-code-assist review (entropy
+ *        = -(p log p) over the vocabulary; the backward reuses the forward
+ *        entropy instead of recomputing it).
+ *   [P3] twinkle pull request #283, "Fix three memory defects in the Megatron
+ *        path", section 1 "selective_log_softmax pins one full-vocab copy per
+ *        row": float32 results for bf16 input; chunked work; softmax
+ *        recomputed in backward rather than saved.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers on the current CUDA device,
+ *     allocated and owned by the caller.  The library never allocates device
+ *     memory (the caller passes a workspace) and keeps no per-call state.
+ *   - Matrices are row-major and contiguous.  hidden, weight (and dhidden)
+ *     must be 16-byte aligned; H must be a multiple of 8.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  A host-detectable error is returned at once
+ *     and nothing is launched.  Errors found on the device (a target out of
+ *     range on a kept row, a pipeline wait that ran out) are recorded in a
+ *     status word inside the workspace; lmhead_get_status() reads it.
+ *   - No C++ exception crosses this boundary and the library never exits the
+ *     process.
+ *   - Outputs are float32 (logprob, entropy, lse, dW) and bf16 (dhidden).
+ *     Results are deterministic: no floating-point atomics are used.
+ */
+#ifndef LMHEAD_H
+#define LMHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LMHEAD_OK = 0,
+  LMHEAD_EINVAL = 1,       /* bad argument: NULL pointer, size, alignment     */
+  LMHEAD_EWORKSPACE = 2,   /* workspace smaller than lmhead_workspace_size()   */
+  LMHEAD_ETARGET = 3,      /* (device) a kept row's target is outside [0, V)   */
+  LMHEAD_ECUDA = 4,        /* a CUDA runtime call failed                       */
+  LMHEAD_ETIMEOUT = 5,     /* (device) a pipeline wait gave up; results invalid*/
+  LMHEAD_EUNSUPPORTED = 6  /* the current device is not an sm_103 GPU          */
+} lmhead_status;
+
+/* Opaque cudaStream_t. */
+typedef void* lmhead_stream_t;
+
+/* Default rows per chunk of kept tokens ([P1] Overview: token chunk 8192). */
+#define LMHEAD_DEFAULT_CHUNK_ROWS 8192
+
+/*
+ * Bytes of device workspace that lmhead_fwd / lmhead_bwd / lmhead_compact
+ * need for these sizes (the same figure serves all three).  chunk_rows <= 0
+ * selects LMHEAD_DEFAULT_CHUNK_ROWS.  The figure grows as
+ * O(N + C*(H + V)) with C = chunk_rows: it never holds [N, V] logits
+ * ([P3] section 1: memory scales with chunks, not with rows).
+ * Returns 0 for invalid sizes (N < 0, H or V < 1).
+ */
+size_t lmhead_workspace_size(int64_t N, int H, int V, int want_entropy, int chunk_rows);
+
+/*
+ * Keep mask after the next-token shift ([P1] Overview).
+ *   loss_mask, ce_weight, kl_weight : float32 [N] token-aligned loss
+ *       components, each nullable (NULL = reads no token).  Any non-zero
+ *       value counts as "read".
+ *   seq_offsets : int32 [n_seq + 1], ascending, seq_offsets[0] = 0 and
+ *       seq_offsets[n_seq] = N: the packed sequences.
+ *   keep (out)  : uint8 [N]; keep[i] = 1 iff row i+1 is in the same sequence
+ *       as row i and some component is non-zero at token i+1.
+ */
+lmhead_status lmhead_build_keep_mask(const float* loss_mask, const float* ce_weight,
+                                     const float* kl_weight, const int32_t* seq_offsets,
+                                     int32_t n_seq, int64_t N, uint8_t* keep,
+                                     lmhead_stream_t stream);
+
+/*
+ * Stable stream compaction of the kept rows ([P1] Overview: "compact").
+ *   keep      : uint8 [N], nullable (NULL = every row kept).
+ *   targets   : int64 [N]; only kept rows are read and must lie in [0, V)
+ *               (else the device status becomes LMHEAD_ETARGET and the
+ *               compacted target is stored as 0).
+ *   idx (out)       : int32 [N]; idx[0..Nk) = kept rows in ascending order.
+ *   targets_c (out) : int32 [N]; targets_c[k] = targets[idx[k]].
+ *   d_nk (out)      : int32 [1] on the device: Nk.
+ *   workspace       : >= lmhead_workspace_size(N, 1, 1, 0, 0) bytes.
+ */
+lmhead_status lmhead_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
+                             int32_t* idx, int32_t* targets_c, int32_t* d_nk,
+                             void* workspace, size_t ws_bytes, lmhead_stream_t stream);
+
+/*
+ * Forward: logprob, entropy and lse of every row ([P2] How it works, [P3]
+ * section 1).  Only the kept rows are projected; the vocab matmul runs on the
+ * tensor cores in bf16 with float32 accumulation and an online-softmax
+ * epilogue, chunk_rows kept rows at a time; no [N, V] buffer exists.
+ *   hidden  : bf16 [N, H]     weight : bf16 [V, H]     targets : int64 [N]
+ *   keep    : uint8 [N], nullable (NULL = all rows kept)
+ *   logprob, lse (out) : float32 [N]
+ *   entropy (out)      : float32 [N]; may be NULL iff want_entropy == 0
+ *                        (then it is not computed).
+ *   Skipped rows get +0.0 in every output.
+ */
+lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* targets,
+                         const uint8_t* keep, int64_t N, int H, int V, int want_entropy,
+                         float* logprob, float* entropy, float* lse, int chunk_rows,
+                         void* workspace, size_t ws_bytes, lmhead_stream_t stream);
+
+/*
+ * Backward of L = sum_i grad_logprob[i] logprob[i] + grad_entropy[i] entropy[i]
+ * ([P2] How it works and gemini-code-assist review; [P3] section 1).  The
+ * logits are recomputed tile by tile from hidden and weight; lse and entropy
+ * are the forward's outputs (not recomputed).
+ *   hidden, weight, targets, keep, N, H, V : as passed to lmhead_fwd.
+ *   lse     : float32 [N] from lmhead_fwd.
+ *   entropy : float32 [N] from lmhead_fwd; read only when grad_entropy is
+ *             given (may be NULL otherwise).
+ *   grad_logprob : float32 [N].
+ *   grad_entropy : float32 [N], nullable: NULL = metric-only entropy, no
+ *             entropy term in the gradient.
+ *   dhidden (out): bf16 [N, H]; rows of skipped tokens are written as 0.
+ *   dweight (out): float32 [V, H]; overwritten when dw_accumulate == 0,
+ *             added to when dw_accumulate != 0 (gradient accumulation).
+ */
+lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* targets,
+                         const uint8_t* keep, int64_t N, int H, int V, const float* lse,
+                         const float* entropy, const float* grad_logprob,
+                         const float* grad_entropy, void* dhidden, float* dweight,
+                         int dw_accumulate, int chunk_rows, void* workspace, size_t ws_bytes,
+                         lmhead_stream_t stream);
+
+/*
+ * Expand compacted per-row values back to all rows ([P1] Overview: expand
+ * back, skipped positions get zeros).
+ *   src  : float32 [Nk]   idx : int32 [Nk] (from lmhead_compact)
+ *   d_nk : int32 [1] on the device (from lmhead_compact)
+ *   dst (out) : float32 [N]; dst[idx[k]] = src[k], +0.0 elsewhere.
+ */
+lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t* d_nk,
+                            int64_t N, float* dst, lmhead_stream_t stream);
+
+/*
+ * Device-side status of the last lmhead_* call that used this workspace:
+ * synchronises `stream`, then returns LMHEAD_OK, LMHEAD_ETARGET or
+ * LMHEAD_ETIMEOUT (or LMHEAD_ECUDA if the stream reports an error).
+ */
+lmhead_status lmhead_get_status(const void* workspace, lmhead_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* lmhead_strerror(lmhead_status status);
+
+/*
+ * Diagnostics (no effect on results).
+ *   lmhead_profile_enable(1) makes later calls record a CUDA event pair around
+ *   every kernel launch; lmhead_profile_read() synchronises on those events
+ *   and reports, per kernel kind k (0 <= k < lmhead_profile_kinds()), the
+ *   launches and their summed device milliseconds since the last read, then
+ *   clears them.  lmhead_profile_kind_name(k) names kind k.
+ *   lmhead_launch_count() is the number of kernels this library has launched
+ *   in the process so far.
+ */
+void lmhead_profile_enable(int on);
+int lmhead_profile_kinds(void);
+const char* lmhead_profile_kind_name(int kind);
+lmhead_status lmhead_profile_read(int64_t* launches, double* total_ms);
+int64_t lmhead_launch_count(void);
+
+/* Library version string. */
+const char* lmhead_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMHEAD_H */

@@ -1,0 +1,24 @@
+"""GB300-native fused LM-head scoring with keep-mask compaction.
+
+The compute path is the CUDA library ``_lib/liblmhead.so`` (sources in
+``csrc/``, C ABI in ``include/lmhead.h``); ``lmhead`` is its thin ctypes
+binding and ``api`` a small convenience layer that allocates outputs and the
+workspace with torch.  ``synth`` draws seeded synthetic inputs.
+"""
+
+from .lmhead import (  # noqa: F401
+    DEFAULT_CHUNK_ROWS,
+    LmheadError,
+    lmhead_build_keep_mask,
+    lmhead_bwd,
+    lmhead_compact,
+    lmhead_expand,
+    lmhead_fwd,
+    lmhead_get_status,
+    lmhead_launch_count,
+    lmhead_profile_enable,
+    lmhead_profile_read,
+    lmhead_strerror,
+    lmhead_version,
+    lmhead_workspace_size,
+)

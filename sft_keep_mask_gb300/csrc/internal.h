@@ -1,0 +1,83 @@
+// Internal interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace lmhead {
+
+// Tile shape of the tcgen05 GEMM: 128 x 256 fp32 accumulator in TMEM,
+// 64-element (128-byte) K steps staged by TMA with the 128-byte swizzle.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kGemmSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256;
+
+// The four contractions of the path.
+//   kFwd: Z = Hc W^T  -> per-row online-softmax partials per 256-column tile
+//   kDz : Z = Hc W^T  -> dZ (bf16) from the recomputed logits
+//   kDh : dHc = dZ W  -> rows scattered to dhidden (bf16)
+//   kDw : dW (+)= dZ^T Hc (fp32)
+enum GemmMode : int { kFwd = 0, kDz = 1, kDh = 2, kDw = 3 };
+
+struct TcGemmParams {
+  const int32_t* d_nk;      // device Nk
+  int chunk_start;          // first compact row of this chunk
+  int chunk_rows;           // C: rows per chunk (multiple of 256)
+  int V;
+  int H;
+  int group_n;              // N tiles per raster group (L2 reuse)
+  int* status;              // device status word
+  // epilogue operands (compact, indexed by compact row)
+  const int32_t* targets_c;
+  const int32_t* idx;
+  const float* lse_c;
+  const float* ent_c;
+  const float* glp_c;
+  const float* gent_c;      // nullable: metric-only entropy
+  int want_entropy;
+  float4* part;             // kFwd: [ceil(V/kBN)][C] (m, s, u, t)
+  __nv_bfloat16* dz;        // kDz: [C, dz_ld]
+  int64_t dz_ld;
+  __nv_bfloat16* dhidden;   // kDh: [N, H]
+  float* dw;                // kDw: [V, H]
+  int beta;                 // kDw: 1 = add to dw
+};
+
+template <int MODE>
+cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
+                           const TcGemmParams& p, int grid, cudaStream_t stream);
+
+// Row kernels (rowops.cu).
+cudaError_t launch_build_keep(const float* c0, const float* c1, const float* c2,
+                              const int32_t* offsets, int n_seq, int64_t N, uint8_t* keep,
+                              cudaStream_t s);
+cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
+                           int32_t* idx, int32_t* targets_c, int32_t* d_nk, int32_t* counts,
+                           int* status, cudaStream_t s);
+cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
+                               const int32_t* d_nk, int chunk_start, int chunk_rows, int H,
+                               __nv_bfloat16* hc, cudaStream_t s);
+cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_start,
+                         int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
+                         float* lse_c, cudaStream_t s);
+cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,
+                           int64_t N, const float* a_c, const float* b_c, const float* c_c,
+                           float* a, float* b, float* c, cudaStream_t s);
+cudaError_t launch_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,
+                          float* dst, cudaStream_t s);
+cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N,
+                              const float* a, const float* b, const float* c, const float* d,
+                              float* a_c, float* b_c, float* c_c, float* d_c, cudaStream_t s);
+cudaError_t launch_zero_skipped_rows(const uint8_t* keep, int64_t N, int H,
+                                     __nv_bfloat16* dhidden, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace lmhead

@@ -1,0 +1,525 @@
+// C-ABI layer of the fused LM-head library: argument checks, the workspace
+// layout, TMA tensor maps, the chunk loop and launch-level profiling.
+// Every kernel it launches is one of this library's own (rowops.cu and the
+// four tcgen05 GEMM instantiations).
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/lmhead.h"
+#include "internal.h"
+
+namespace lmhead {
+namespace {
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+inline int64_t cdiv(int64_t x, int64_t m) { return (x + m - 1) / m; }
+
+// ------------------------------------------------------------ workspace
+// Regions are 256-byte aligned offsets from the workspace base.
+struct Layout {
+  int64_t C = 0;        // rows per chunk (multiple of 256)
+  int64_t num_vt = 0;   // 256-wide vocab tiles
+  int64_t dz_ld = 0;    // row stride of the dZ chunk buffer (elements)
+  size_t hdr = 0, counts = 0, idx = 0, yc = 0, v0 = 0, v1 = 0, v2 = 0, v3 = 0, hc = 0, part = 0,
+         dz = 0, total = 0;
+};
+
+Layout make_layout(int64_t N, int H, int V, int chunk_rows) {
+  Layout L;
+  int64_t c = chunk_rows > 0 ? chunk_rows : LMHEAD_DEFAULT_CHUNK_ROWS;
+  if (c > N) c = N;
+  L.C = round_up(c < 1 ? 1 : c, 256);
+  L.num_vt = cdiv(V, kBN);
+  L.dz_ld = round_up(V, 8);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += static_cast<size_t>(round_up(static_cast<int64_t>(bytes), 256));
+    return at;
+  };
+  L.hdr = take(256);
+  L.counts = take(static_cast<size_t>(cdiv(N, 4096) + 1) * 4);
+  L.idx = take(static_cast<size_t>(N) * 4);
+  L.yc = take(static_cast<size_t>(N) * 4);
+  L.v0 = take(static_cast<size_t>(N) * 4);
+  L.v1 = take(static_cast<size_t>(N) * 4);
+  L.v2 = take(static_cast<size_t>(N) * 4);
+  L.v3 = take(static_cast<size_t>(N) * 4);
+  L.hc = take(static_cast<size_t>(L.C) * H * 2);
+  L.part = take(static_cast<size_t>(L.num_vt) * L.C * 16);
+  L.dz = take(static_cast<size_t>(L.C) * L.dz_ld * 2);
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ------------------------------------------------------------ profiling
+enum Kind : int {
+  kKindBuildKeep = 0, kKindCompact, kKindGatherRows, kKindGemmFwd, kKindMerge, kKindExpand,
+  kKindGatherVec, kKindZeroRows, kKindGemmDz, kKindGemmDh, kKindGemmDw, kNumKinds
+};
+const char* kKindNames[kNumKinds] = {"build_keep", "compact",  "gather_rows", "gemm_fwd",
+                                     "merge",      "expand",   "gather_vec",  "zero_rows",
+                                     "gemm_dz",    "gemm_dh",  "gemm_dw"};
+
+std::atomic<int64_t> g_launches{0};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+struct Rec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::vector<Rec> g_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one kernel launch: counts it and, when profiling is on, records
+// an event pair around it on the launching stream.
+class Launch {
+ public:
+  Launch(int kind, cudaStream_t s, int nkernels = 1) : kind_(kind), s_(s) {
+    g_launches.fetch_add(nkernels);
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (g_prof_on) {
+      a_ = take_event();
+      b_ = take_event();
+      cudaEventRecord(a_, s_);
+    }
+  }
+  ~Launch() {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (a_ != nullptr) {
+      cudaEventRecord(b_, s_);
+      g_recs.push_back({kind_, a_, b_});
+    }
+  }
+
+ private:
+  int kind_;
+  cudaStream_t s_;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+// ------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
+// `ld` elements; boxes of [box_rows, box_cols] with the 128-byte swizzle
+// (box_cols * 2 == 128).  Out-of-range elements load as zero.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
+              int box_rows, int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ device info
+struct DevInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+DevInfo device_info() {
+  static DevInfo cache[64];
+  static bool have[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevInfo{};
+  std::lock_guard<std::mutex> g(mu);
+  if (!have[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].sms = sms;
+    cache[dev].ok = (major == 10 && minor == 3);
+    have[dev] = true;
+  }
+  return cache[dev];
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lmhead_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LMHEAD_OK : LMHEAD_ECUDA; }
+
+#define LM_TRY(expr)                                  \
+  do {                                                \
+    cudaError_t e_ = (expr);                          \
+    if (e_ != cudaSuccess) return LMHEAD_ECUDA;       \
+  } while (0)
+
+lmhead_status check_sizes(int64_t N, int H, int V) {
+  if (N < 0 || N > (int64_t{1} << 31) - 1024) return LMHEAD_EINVAL;
+  if (H < 8 || (H % 8) != 0 || V < 1) return LMHEAD_EINVAL;
+  return LMHEAD_OK;
+}
+
+lmhead_status check_ws(void* ws, size_t ws_bytes, const Layout& L) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LMHEAD_EINVAL;
+  if (ws_bytes < L.total) return LMHEAD_EWORKSPACE;
+  return LMHEAD_OK;
+}
+
+lmhead_status run_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
+                          int32_t* idx, int32_t* yc, int32_t* d_nk, int32_t* counts, int* status,
+                          cudaStream_t s) {
+  if (N == 0) {
+    LM_TRY(cudaMemsetAsync(d_nk, 0, sizeof(int32_t), s));
+    return LMHEAD_OK;
+  }
+  Launch l(kKindCompact, s, 2);
+  LM_TRY(launch_compact(keep, targets, N, V, idx, yc, d_nk, counts, status, s));
+  return LMHEAD_OK;
+}
+
+int gemm_grid(int64_t tiles) {
+  const int sms = device_info().sms;
+  return static_cast<int>(tiles < sms ? (tiles < 1 ? 1 : tiles) : sms);
+}
+
+}  // namespace
+
+int device_sm_count() { return device_info().sms; }
+
+}  // namespace lmhead
+
+using namespace lmhead;
+
+extern "C" {
+
+size_t lmhead_workspace_size(int64_t N, int H, int V, int want_entropy, int chunk_rows) {
+  (void)want_entropy;
+  if (N < 0 || H < 1 || V < 1) return 0;
+  return make_layout(N, H, V, chunk_rows).total;
+}
+
+lmhead_status lmhead_build_keep_mask(const float* loss_mask, const float* ce_weight,
+                                     const float* kl_weight, const int32_t* seq_offsets,
+                                     int32_t n_seq, int64_t N, uint8_t* keep,
+                                     lmhead_stream_t stream) {
+  if (N < 0 || n_seq < 0 || seq_offsets == nullptr || keep == nullptr) return LMHEAD_EINVAL;
+  if (N == 0) return LMHEAD_OK;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch l(kKindBuildKeep, s);
+  return cuda_status(launch_build_keep(loss_mask, ce_weight, kl_weight, seq_offsets, n_seq, N,
+                                       keep, s));
+}
+
+lmhead_status lmhead_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
+                             int32_t* idx, int32_t* targets_c, int32_t* d_nk, void* workspace,
+                             size_t ws_bytes, lmhead_stream_t stream) {
+  if (N < 0 || V < 1 || targets == nullptr || idx == nullptr || targets_c == nullptr ||
+      d_nk == nullptr)
+    return LMHEAD_EINVAL;
+  const Layout L = make_layout(N, 8, V, 256);
+  const size_t need = L.counts + static_cast<size_t>(round_up((cdiv(N, 4096) + 1) * 4, 256));
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return LMHEAD_EINVAL;
+  if (ws_bytes < need) return LMHEAD_EWORKSPACE;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(workspace, L.hdr);
+  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  return run_compact(keep, targets, N, V, idx, targets_c, d_nk, at<int32_t>(workspace, L.counts),
+                     status, s);
+}
+
+lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* targets,
+                         const uint8_t* keep, int64_t N, int H, int V, int want_entropy,
+                         float* logprob, float* entropy, float* lse, int chunk_rows,
+                         void* workspace, size_t ws_bytes, lmhead_stream_t stream) {
+  lmhead_status st = check_sizes(N, H, V);
+  if (st != LMHEAD_OK) return st;
+  if (hidden == nullptr || weight == nullptr || targets == nullptr || logprob == nullptr ||
+      lse == nullptr || (want_entropy && entropy == nullptr))
+    return LMHEAD_EINVAL;
+  if (!aligned16(hidden) || !aligned16(weight)) return LMHEAD_EINVAL;
+  const Layout L = make_layout(N, H, V, chunk_rows);
+  st = check_ws(workspace, ws_bytes, L);
+  if (st != LMHEAD_OK) return st;
+  if (N == 0) return LMHEAD_OK;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  int* status = at<int>(workspace, L.hdr);
+  int32_t* d_nk = status + 1;
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  int32_t* yc = at<int32_t>(workspace, L.yc);
+  float* lp_c = at<float>(workspace, L.v0);
+  float* ent_c = at<float>(workspace, L.v1);
+  float* lse_c = at<float>(workspace, L.v2);
+  __nv_bfloat16* hc = at<__nv_bfloat16>(workspace, L.hc);
+  float4* part = at<float4>(workspace, L.part);
+
+  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  st = run_compact(keep, targets, N, V, idx, yc, d_nk, at<int32_t>(workspace, L.counts), status,
+                   s);
+  if (st != LMHEAD_OK) return st;
+
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, hc, L.C, H, H, kBM, 64) ||
+      !make_map(&mb, weight, V, H, H, kBN, 64))
+    return LMHEAD_ECUDA;
+
+  TcGemmParams p{};
+  p.d_nk = d_nk;
+  p.chunk_rows = static_cast<int>(L.C);
+  p.V = V;
+  p.H = H;
+  p.group_n = 16;
+  p.status = status;
+  p.targets_c = yc;
+  p.want_entropy = want_entropy ? 1 : 0;
+  p.part = part;
+  const int grid = gemm_grid(cdiv(L.C, kBM) * L.num_vt);
+
+  for (int64_t cs = 0; cs < N; cs += L.C) {
+    {
+      Launch l(kKindGatherRows, s);
+      LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
+                                static_cast<int>(cs), static_cast<int>(L.C), H, hc, s));
+    }
+    p.chunk_start = static_cast<int>(cs);
+    {
+      Launch l(kKindGemmFwd, s);
+      LM_TRY(launch_tc_gemm<kFwd>(ma, mb, p, grid, s));
+    }
+    {
+      Launch l(kKindMerge, s);
+      LM_TRY(launch_merge(part, static_cast<int>(L.num_vt), d_nk, static_cast<int>(cs),
+                          static_cast<int>(L.C), p.want_entropy, lp_c, ent_c, lse_c, s));
+    }
+  }
+  {
+    Launch l(kKindExpand, s);
+    LM_TRY(launch_expand3(keep, idx, d_nk, N, lp_c, want_entropy ? ent_c : nullptr, lse_c,
+                          logprob, want_entropy ? entropy : nullptr, lse, s));
+  }
+  return LMHEAD_OK;
+}
+
+lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* targets,
+                         const uint8_t* keep, int64_t N, int H, int V, const float* lse,
+                         const float* entropy, const float* grad_logprob,
+                         const float* grad_entropy, void* dhidden, float* dweight,
+                         int dw_accumulate, int chunk_rows, void* workspace, size_t ws_bytes,
+                         lmhead_stream_t stream) {
+  lmhead_status st = check_sizes(N, H, V);
+  if (st != LMHEAD_OK) return st;
+  if (hidden == nullptr || weight == nullptr || targets == nullptr || lse == nullptr ||
+      grad_logprob == nullptr || dhidden == nullptr || dweight == nullptr ||
+      (grad_entropy != nullptr && entropy == nullptr))
+    return LMHEAD_EINVAL;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(dhidden) || !aligned16(dweight))
+    return LMHEAD_EINVAL;
+  const Layout L = make_layout(N, H, V, chunk_rows);
+  st = check_ws(workspace, ws_bytes, L);
+  if (st != LMHEAD_OK) return st;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    if (!dw_accumulate)
+      LM_TRY(cudaMemsetAsync(dweight, 0, static_cast<size_t>(V) * H * sizeof(float), s));
+    return LMHEAD_OK;
+  }
+
+  int* status = at<int>(workspace, L.hdr);
+  int32_t* d_nk = status + 1;
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  int32_t* yc = at<int32_t>(workspace, L.yc);
+  float* lse_c = at<float>(workspace, L.v0);
+  float* ent_c = at<float>(workspace, L.v1);
+  float* glp_c = at<float>(workspace, L.v2);
+  float* gent_c = at<float>(workspace, L.v3);
+  __nv_bfloat16* hc = at<__nv_bfloat16>(workspace, L.hc);
+  __nv_bfloat16* dz = at<__nv_bfloat16>(workspace, L.dz);
+
+  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  st = run_compact(keep, targets, N, V, idx, yc, d_nk, at<int32_t>(workspace, L.counts), status,
+                   s);
+  if (st != LMHEAD_OK) return st;
+  {
+    Launch l(kKindGatherVec, s);
+    LM_TRY(launch_gather_vec(idx, d_nk, N, lse, grad_entropy ? entropy : nullptr, grad_logprob,
+                             grad_entropy, lse_c, ent_c, glp_c, gent_c, s));
+  }
+  if (keep != nullptr) {
+    Launch l(kKindZeroRows, s);
+    LM_TRY(launch_zero_skipped_rows(keep, N, H, static_cast<__nv_bfloat16*>(dhidden), s));
+  }
+
+  CUtensorMap m_hc_k, m_w_k, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn;
+  if (!make_map(&m_hc_k, hc, L.C, H, H, kBM, 64) ||        // A of kDz (K-major)
+      !make_map(&m_w_k, weight, V, H, H, kBN, 64) ||       // B of kDz (K-major)
+      !make_map(&m_dz_k, dz, L.C, V, L.dz_ld, kBM, 64) ||  // A of kDh (K-major)
+      !make_map(&m_w_mn, weight, V, H, H, 64, 64) ||       // B of kDh (MN-major boxes)
+      !make_map(&m_dz_mn, dz, L.C, V, L.dz_ld, 64, 64) ||  // A of kDw (MN-major boxes)
+      !make_map(&m_hc_mn, hc, L.C, H, H, 64, 64))          // B of kDw (MN-major boxes)
+    return LMHEAD_ECUDA;
+
+  TcGemmParams p{};
+  p.d_nk = d_nk;
+  p.chunk_rows = static_cast<int>(L.C);
+  p.V = V;
+  p.H = H;
+  p.status = status;
+  p.targets_c = yc;
+  p.idx = idx;
+  p.lse_c = lse_c;
+  p.ent_c = ent_c;
+  p.glp_c = glp_c;
+  p.gent_c = grad_entropy ? gent_c : nullptr;
+  p.want_entropy = grad_entropy ? 1 : 0;
+  p.dz = dz;
+  p.dz_ld = L.dz_ld;
+  p.dhidden = static_cast<__nv_bfloat16*>(dhidden);
+  p.dw = dweight;
+  const int64_t n_h_tiles = cdiv(H, kBN);
+  const int grid_dz = gemm_grid(cdiv(L.C, kBM) * L.num_vt);
+  const int grid_dh = gemm_grid(cdiv(L.C, kBM) * n_h_tiles);
+  const int grid_dw = gemm_grid(cdiv(V, kBM) * n_h_tiles);
+
+  for (int64_t cs = 0; cs < N; cs += L.C) {
+    p.chunk_start = static_cast<int>(cs);
+    {
+      Launch l(kKindGatherRows, s);
+      LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
+                                static_cast<int>(cs), static_cast<int>(L.C), H, hc, s));
+    }
+    {
+      Launch l(kKindGemmDz, s);
+      p.group_n = 16;
+      LM_TRY(launch_tc_gemm<kDz>(m_hc_k, m_w_k, p, grid_dz, s));
+    }
+    {
+      Launch l(kKindGemmDh, s);
+      p.group_n = static_cast<int>(n_h_tiles);
+      LM_TRY(launch_tc_gemm<kDh>(m_dz_k, m_w_mn, p, grid_dh, s));
+    }
+    {
+      Launch l(kKindGemmDw, s);
+      p.group_n = static_cast<int>(n_h_tiles);
+      p.beta = (cs > 0 || dw_accumulate) ? 1 : 0;
+      LM_TRY(launch_tc_gemm<kDw>(m_dz_mn, m_hc_mn, p, grid_dw, s));
+    }
+  }
+  return LMHEAD_OK;
+}
+
+lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,
+                            float* dst, lmhead_stream_t stream) {
+  if (N < 0 || src == nullptr || idx == nullptr || d_nk == nullptr || dst == nullptr)
+    return LMHEAD_EINVAL;
+  if (N == 0) return LMHEAD_OK;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch l(kKindExpand, s);
+  return cuda_status(launch_expand(src, idx, d_nk, N, dst, s));
+}
+
+lmhead_status lmhead_get_status(const void* workspace, lmhead_stream_t stream) {
+  if (workspace == nullptr) return LMHEAD_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LMHEAD_ECUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LMHEAD_ECUDA;
+  return static_cast<lmhead_status>(h);
+}
+
+const char* lmhead_strerror(lmhead_status status) {
+  switch (status) {
+    case LMHEAD_OK: return "ok";
+    case LMHEAD_EINVAL: return "invalid argument";
+    case LMHEAD_EWORKSPACE: return "workspace too small";
+    case LMHEAD_ETARGET: return "target outside [0, V) on a kept row";
+    case LMHEAD_ECUDA: return "CUDA runtime error";
+    case LMHEAD_ETIMEOUT: return "device pipeline wait timed out";
+    case LMHEAD_EUNSUPPORTED: return "device is not an sm_103 GPU";
+  }
+  return "unknown status";
+}
+
+void lmhead_profile_enable(int on) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+int lmhead_profile_kinds(void) { return kNumKinds; }
+
+const char* lmhead_profile_kind_name(int kind) {
+  return (kind >= 0 && kind < kNumKinds) ? kKindNames[kind] : "";
+}
+
+lmhead_status lmhead_profile_read(int64_t* launches, double* total_ms) {
+  if (launches == nullptr || total_ms == nullptr) return LMHEAD_EINVAL;
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (int k = 0; k < kNumKinds; ++k) {
+    launches[k] = 0;
+    total_ms[k] = 0.0;
+  }
+  lmhead_status st = LMHEAD_OK;
+  for (const Rec& r : g_recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      st = LMHEAD_ECUDA;
+    launches[r.kind] += 1;
+    total_ms[r.kind] += ms;
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  return st;
+}
+
+int64_t lmhead_launch_count(void) { return g_launches.load(); }
+
+const char* lmhead_version(void) { return "lmhead-gb300 0.1.0 (sm_103a, tcgen05)"; }
+
+}  // extern "C"

@@ -1,0 +1,306 @@
+// Row kernels of the fused LM-head path: keep-mask construction, stable
+// compaction of the kept rows, gathers into compact buffers, the split-V
+// partial merge and the expansion back to every row.  All of them are
+// memory-bound and sized by the device-resident number of kept rows, so no
+// host synchronisation is needed between the steps.
+//
+// Source for the steps: prime-rl pull request #3326, "Don't compute the
+// logprobs and their gradients for tokens no loss component reads",
+// "Overview" (keep mask after the next-token shift; compact -> chunked
+// logprob/entropy -> expand back with zeros).
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lmhead {
+
+namespace {
+
+constexpr int kScanThreads = 256;
+constexpr int kScanPerThread = 16;
+constexpr int kScanTile = kScanThreads * kScanPerThread;  // rows per block
+
+// ---------------------------------------------------------------- keep mask
+__global__ void build_keep_kernel(const float* __restrict__ c0, const float* __restrict__ c1,
+                                  const float* __restrict__ c2,
+                                  const int32_t* __restrict__ offsets, int n_seq, int64_t N,
+                                  uint8_t* __restrict__ keep) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const int64_t nxt = i + 1;
+  uint8_t k = 0;
+  if (nxt < N) {
+    // Is token i+1 the first token of a packed sequence?  (binary search)
+    int lo = 0, hi = n_seq;  // offsets[0..n_seq]
+    bool starts = false;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      const int64_t v = offsets[mid];
+      if (v == nxt) { starts = true; break; }
+      if (v < nxt) lo = mid + 1; else hi = mid - 1;
+    }
+    if (!starts) {
+      const bool read = (c0 != nullptr && c0[nxt] != 0.f) || (c1 != nullptr && c1[nxt] != 0.f) ||
+                        (c2 != nullptr && c2[nxt] != 0.f);
+      k = read ? 1 : 0;
+    }
+  }
+  keep[i] = k;
+}
+
+// --------------------------------------------------------------- compaction
+__device__ __forceinline__ int block_sum(int v, int* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  int tot = 0;
+  for (int j = 0; j < (int)(blockDim.x >> 5); ++j) tot += red[j];
+  return tot;
+}
+
+// Per block of kScanTile rows: the number of kept rows.
+__global__ void count_kernel(const uint8_t* __restrict__ keep, int64_t N, int32_t* counts) {
+  __shared__ int red[kScanThreads / 32];
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kScanTile;
+  int c = 0;
+  for (int j = 0; j < kScanPerThread; ++j) {
+    const int64_t r = base + threadIdx.x + static_cast<int64_t>(j) * kScanThreads;
+    if (r < N) c += (keep == nullptr || keep[r] != 0) ? 1 : 0;
+  }
+  const int tot = block_sum(c, red);
+  if (threadIdx.x == 0) counts[blockIdx.x] = tot;
+}
+
+// Writes the kept rows of block b, in order, after the kept rows of blocks
+// 0..b-1; the last block also writes Nk.
+__global__ void scatter_kernel(const uint8_t* __restrict__ keep,
+                               const int64_t* __restrict__ targets, int64_t N, int V,
+                               const int32_t* __restrict__ counts, int32_t* __restrict__ idx,
+                               int32_t* __restrict__ targets_c, int32_t* d_nk, int* status) {
+  __shared__ int red[kScanThreads / 32];
+  __shared__ int warp_tot[kScanThreads / 32];
+  // offset of this block = sum of the counts of the blocks before it
+  int pre = 0;
+  for (int j = threadIdx.x; j < static_cast<int>(blockIdx.x); j += kScanThreads) pre += counts[j];
+  const int offset = block_sum(pre, red);
+
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kScanTile +
+                       static_cast<int64_t>(threadIdx.x) * kScanPerThread;
+  uint32_t bits = 0;
+  for (int j = 0; j < kScanPerThread; ++j) {
+    const int64_t r = base + j;
+    if (r < N && (keep == nullptr || keep[r] != 0)) bits |= 1u << j;
+  }
+  const int mine = __popc(bits);
+  // exclusive scan of `mine` over the block
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  int incl = mine;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (l >= o) incl += v;
+  }
+  if (l == 31) warp_tot[w] = incl;
+  __syncthreads();
+  int wpre = 0;
+  for (int j = 0; j < w; ++j) wpre += warp_tot[j];
+  int pos = offset + wpre + incl - mine;
+  for (int j = 0; j < kScanPerThread; ++j) {
+    if (bits & (1u << j)) {
+      const int64_t r = base + j;
+      int64_t y = targets[r];
+      if (y < 0 || y >= V) {
+        atomicCAS(status, 0, kStatusTarget);
+        y = 0;
+      }
+      idx[pos] = static_cast<int32_t>(r);
+      targets_c[pos] = static_cast<int32_t>(y);
+      ++pos;
+    }
+  }
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == kScanThreads - 1) {
+    int tot = 0;
+    for (int j = 0; j < kScanThreads / 32; ++j) tot += warp_tot[j];
+    *d_nk = offset + tot;
+  }
+}
+
+// ------------------------------------------------------------------ gathers
+// h_c[r] = hidden[idx[chunk_start + r]] for r < rows in chunk; rows up to the
+// next multiple of 256 are zero-filled (they enter the weight-gradient
+// contraction as zero K rows).  One warp per row, 16-byte vectors.
+__global__ void gather_rows_kernel(const uint4* __restrict__ hidden,
+                                   const int32_t* __restrict__ idx, const int32_t* d_nk,
+                                   int chunk_start, int chunk_rows, int vec_per_row,
+                                   uint4* __restrict__ hc) {
+  const int nk = *d_nk;
+  int rows = nk - chunk_start;
+  rows = rows < 0 ? 0 : (rows > chunk_rows ? chunk_rows : rows);
+  const int padded = (rows + 255) & ~255;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int l = threadIdx.x & 31;
+  if (r >= padded || rows == 0) return;
+  uint4* dst = hc + static_cast<int64_t>(r) * vec_per_row;
+  if (r < rows) {
+    const uint4* src = hidden + static_cast<int64_t>(idx[chunk_start + r]) * vec_per_row;
+    for (int v = l; v < vec_per_row; v += 32) dst[v] = src[v];
+  } else {
+    for (int v = l; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void gather_vec_kernel(const int32_t* __restrict__ idx, const int32_t* d_nk,
+                                  const float* a, const float* b, const float* c, const float* d,
+                                  float* a_c, float* b_c, float* c_c, float* d_c) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= *d_nk) return;
+  const int r = idx[k];
+  if (a) a_c[k] = a[r];
+  if (b) b_c[k] = b[r];
+  if (c) c_c[k] = c[r];
+  if (d) d_c[k] = d[r];
+}
+
+// -------------------------------------------------------------------- merge
+// Split-V merge of the per-tile (m, s, u, t) partials of one chunk:
+//   M = max m_i, S = sum s_i e^(m_i - M), U = sum e^(m_i - M)(u_i + s_i (m_i - M))
+//   lse = M + log S, logprob = t - lse, entropy = log S - U / S.
+__global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const int32_t* d_nk,
+                             int chunk_start, int chunk_rows, int want_entropy,
+                             float* __restrict__ lp_c, float* __restrict__ ent_c,
+                             float* __restrict__ lse_c) {
+  const int nk = *d_nk;
+  int rows = nk - chunk_start;
+  rows = rows < 0 ? 0 : (rows > chunk_rows ? chunk_rows : rows);
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  float M = -INFINITY;
+  for (int v = 0; v < num_vt; ++v) M = fmaxf(M, part[static_cast<int64_t>(v) * chunk_rows + r].x);
+  float S = 0.f, U = 0.f, T = -INFINITY;
+  for (int v = 0; v < num_vt; ++v) {
+    const float4 q = part[static_cast<int64_t>(v) * chunk_rows + r];
+    const float sc = expf(q.x - M);
+    S = fmaf(q.y, sc, S);
+    U = fmaf(sc, fmaf(q.y, q.x - M, q.z), U);
+    T = fmaxf(T, q.w);
+  }
+  const float logS = logf(S);
+  const float lse = M + logS;
+  lp_c[chunk_start + r] = T - lse;
+  lse_c[chunk_start + r] = lse;
+  if (want_entropy) ent_c[chunk_start + r] = logS - U / S;
+}
+
+// ------------------------------------------------------------------- expand
+// Disjoint writes: skipped rows get +0.0, kept row idx[k] gets value k.
+__global__ void expand3_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ idx,
+                               const int32_t* d_nk, int64_t N, const float* a_c,
+                               const float* b_c, const float* c_c, float* a, float* b,
+                               float* c) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  if (keep != nullptr && keep[i] == 0) {
+    if (a) a[i] = 0.f;
+    if (b) b[i] = 0.f;
+    if (c) c[i] = 0.f;
+  }
+  if (i < *d_nk) {
+    const int r = idx[i];
+    if (a) a[r] = a_c[i];
+    if (b) b[r] = b_c[i];
+    if (c) c[r] = c_c[i];
+  }
+}
+
+__global__ void scatter_vals_kernel(const float* __restrict__ src, const int32_t* __restrict__ idx,
+                                    const int32_t* d_nk, float* __restrict__ dst) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k < *d_nk) dst[idx[k]] = src[k];
+}
+
+// Rows of skipped tokens of dhidden are written as zeros (warp per row).
+__global__ void zero_skipped_rows_kernel(const uint8_t* __restrict__ keep, int64_t N,
+                                         int vec_per_row, uint4* __restrict__ dh) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= N || keep[r] != 0) return;
+  uint4* dst = dh + r * vec_per_row;
+  for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+}
+
+inline unsigned blocks_for(int64_t n, int per) {
+  return static_cast<unsigned>((n + per - 1) / per);
+}
+
+}  // namespace
+
+cudaError_t launch_build_keep(const float* c0, const float* c1, const float* c2,
+                              const int32_t* offsets, int n_seq, int64_t N, uint8_t* keep,
+                              cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  build_keep_kernel<<<blocks_for(N, 256), 256, 0, s>>>(c0, c1, c2, offsets, n_seq, N, keep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
+                           int32_t* idx, int32_t* targets_c, int32_t* d_nk, int32_t* counts,
+                           int* status, cudaStream_t s) {
+  const unsigned nb = blocks_for(N, kScanTile);
+  count_kernel<<<nb, kScanThreads, 0, s>>>(keep, N, counts);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  scatter_kernel<<<nb, kScanThreads, 0, s>>>(keep, targets, N, V, counts, idx, targets_c, d_nk,
+                                             status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
+                               const int32_t* d_nk, int chunk_start, int chunk_rows, int H,
+                               __nv_bfloat16* hc, cudaStream_t s) {
+  const int vec = H / 8;
+  gather_rows_kernel<<<blocks_for(chunk_rows, 8), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(hidden), idx, d_nk, chunk_start, chunk_rows, vec,
+      reinterpret_cast<uint4*>(hc));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_start,
+                         int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
+                         float* lse_c, cudaStream_t s) {
+  merge_kernel<<<blocks_for(chunk_rows, 128), 128, 0, s>>>(part, num_vt, d_nk, chunk_start,
+                                                           chunk_rows, want_entropy, lp_c, ent_c,
+                                                           lse_c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,
+                           int64_t N, const float* a_c, const float* b_c, const float* c_c,
+                           float* a, float* b, float* c, cudaStream_t s) {
+  expand3_kernel<<<blocks_for(N, 256), 256, 0, s>>>(keep, idx, d_nk, N, a_c, b_c, c_c, a, b, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,
+                          float* dst, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(dst, 0, static_cast<size_t>(N) * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  scatter_vals_kernel<<<blocks_for(N, 256), 256, 0, s>>>(src, idx, d_nk, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N, const float* a,
+                              const float* b, const float* c, const float* d, float* a_c,
+                              float* b_c, float* c_c, float* d_c, cudaStream_t s) {
+  gather_vec_kernel<<<blocks_for(N, 256), 256, 0, s>>>(idx, d_nk, a, b, c, d, a_c, b_c, c_c, d_c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_skipped_rows(const uint8_t* keep, int64_t N, int H,
+                                     __nv_bfloat16* dhidden, cudaStream_t s) {
+  zero_skipped_rows_kernel<<<blocks_for(N, 8), 256, 0, s>>>(keep, N, H / 8,
+                                                           reinterpret_cast<uint4*>(dhidden));
+  return cudaGetLastError();
+}
+
+}  // namespace lmhead

@@ -1,0 +1,447 @@
+// Persistent tcgen05 GEMM for the four contractions of the fused LM head,
+// with the epilogue of each contraction fused in.
+//
+// D[M, N] = A[M, K] * B[N, K]^T, bf16 operands staged in shared memory by TMA
+// (128-byte swizzle), fp32 accumulator in tensor memory.  One CTA per SM; it
+// walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+//
+//   warp 0      TMA producer: a ring of kStages (A, B) stages
+//   warp 1      TMEM owner and MMA issuer (one thread): 4 MMAs of
+//               128 x 256 x 16 per 64-wide K step, into one of two 256-column
+//               accumulators, so the epilogue of tile i overlaps the MMAs of
+//               tile i+1
+//   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. one
+//               accumulator row per thread, 32 columns per tcgen05.ld
+//
+// Operand majors per contraction (K-major = K contiguous in global memory):
+//   kFwd, kDz : A = Hc [rows, H] K-major,  B = W [V, H] K-major
+//   kDh       : A = dZ [rows, V] K-major,  B = W [V, H] MN-major (H contiguous)
+//   kDw       : A = dZ [rows, V] MN-major (V contiguous),
+//               B = Hc [rows, H] MN-major (H contiguous)
+//
+// The logits never leave the SM in the forward: the kFwd epilogue reduces
+// each 128 x 256 tile to per-row (max, sum exp, sum exp * (z - max), target
+// logit) -- the single fused projection of SkyRL pull request #2374
+// ("How it works"), with the entropy -(p log p) of its gemini-code-assist
+// review accumulated online in a numerically safe form.
+#pragma once
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lmhead {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_n, int& mt,
+                                            int& nt) {
+  const int per_group = num_m * group_n;
+  const int g = t / per_group;
+  const int local = t - g * per_group;
+  const int rem = num_n - g * group_n;
+  const int gn = rem < group_n ? rem : group_n;
+  mt = local / gn;
+  nt = g * group_n + (local - (local / gn) * gn);
+}
+
+// Wait without the abort check: used only to drain copies / MMAs in flight
+// before the CTA releases its shared and tensor memory.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                   const __grid_constant__ CUtensorMap tma_b, const TcGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Problem extents; the number of kept rows lives on the device.
+  const int nk = *p.d_nk;
+  int rows_valid = nk - p.chunk_start;
+  rows_valid = rows_valid < 0 ? 0 : (rows_valid > p.chunk_rows ? p.chunk_rows : rows_valid);
+  int M, N, K;
+  if (MODE == kDw) {
+    M = p.V; N = p.H; K = rows_valid;
+    if (rows_valid == 0 && (p.beta || p.chunk_start > 0)) return;
+  } else if (MODE == kDh) {
+    M = rows_valid; N = p.H; K = p.V;
+    if (rows_valid == 0) return;
+  } else {
+    M = rows_valid; N = p.V; K = p.H;
+    if (rows_valid == 0) return;
+  }
+  const int num_m = (M + kBM - 1) / kBM;
+  const int num_n = (N + kBN - 1) / kBN;
+  const int num_kb = (K + kBK - 1) / kBK;
+  const int num_tiles = num_m * num_n;
+  if (static_cast<int>(blockIdx.x) >= num_tiles) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, num_m, num_n, p.group_n, mt, nt);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
+          uint8_t* a_dst = sA + stage * kABytes;
+          uint8_t* b_dst = sB + stage * kBBytes;
+          const int k0 = kb * kBK;
+          if (MODE == kDw) {
+            // A MN-major: dZ[k rows, m cols]; two 64-column boxes
+            tma_load_2d(a_dst, &tma_a, &full[stage], mt * kBM, k0);
+            tma_load_2d(a_dst + 8192, &tma_a, &full[stage], mt * kBM + 64, k0);
+          } else {
+            tma_load_2d(a_dst, &tma_a, &full[stage], k0, mt * kBM);
+          }
+          if (MODE == kDh || MODE == kDw) {
+            // B MN-major: [k rows, n cols]; four 64-column boxes
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(b_dst + j * 8192, &tma_b, &full[stage], nt * kBN + 64 * j, k0);
+          } else {
+            tma_load_2d(b_dst, &tma_b, &full[stage], k0, nt * kBN);
+          }
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // Let every load that was issued land before the CTA exits.
+      for (int s = 0; s < kStages; ++s) {
+        const uint32_t uses = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
+        if (uses > 0) mbar_wait_drain(&full[s], (uses - 1u) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr bool a_mn = (MODE == kDw);
+      constexpr bool b_mn = (MODE == kDh || MODE == kDw);
+      constexpr uint32_t idesc = idesc_bf16(kBM, kBN, a_mn, b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok && num_kb > 0; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_addr(sA + stage * kABytes);
+          const uint32_t b_addr = smem_addr(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+      // No MMA may still be running when the accumulators are released.
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_local = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      int mt, nt;
+      tile_coords(t, num_m, num_n, p.group_n, mt, nt);
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      if (num_kb > 0) {
+        if (!mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+      }
+      const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
+      const int col_tile = nt * kBN;
+
+      if (MODE == kFwd) {
+        const int row = mt * kBM + row_local;  // row within the chunk
+        const bool row_ok = row < rows_valid;
+        const int y = row_ok ? p.targets_c[p.chunk_start + row] : -1;
+        const bool tail = col_tile + kBN > p.V;
+        float m2 = -INFINITY, s = 0.f, u2 = 0.f, tz = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait();
+          if (c == kBN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+          const int col = col_tile + c * 32;
+          float z[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]);
+          if (tail) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col + j >= p.V) z[j] = -INFINITY;
+          }
+          if (static_cast<unsigned>(y - col) < 32u) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j == y - col) tz = z[j];
+          }
+          float cmax = z[0];
+#pragma unroll
+          for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, z[j]);
+          if (cmax == -INFINITY) continue;  // chunk wholly past the vocabulary
+          const float cm2 = cmax * kLog2e;
+          if (cm2 > m2) {
+            if (m2 != -INFINITY) {
+              const float sc = fast_exp2(m2 - cm2);
+              u2 = sc * (u2 + s * (m2 - cm2));
+              s *= sc;
+            }
+            m2 = cm2;
+          }
+          if (!tail) {
+            if (p.want_entropy) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float d = fmaf(z[j], kLog2e, -m2);
+                const float e = fast_exp2(d);
+                s += e;
+                u2 = fmaf(e, d, u2);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) s += fast_exp2(fmaf(z[j], kLog2e, -m2));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (col + j < p.V) {
+                const float d = fmaf(z[j], kLog2e, -m2);
+                const float e = fast_exp2(d);
+                s += e;
+                u2 = fmaf(e, d, u2);
+              }
+            }
+          }
+        }
+        if (row_ok)
+          p.part[static_cast<int64_t>(nt) * p.chunk_rows + row] =
+              make_float4(m2 * kLn2, s, u2 * kLn2, tz);
+      } else if (MODE == kDz) {
+        const int row = mt * kBM + row_local;
+        const bool row_ok = row < rows_valid;
+        float lse2 = 0.f, ca = 0.f, cb = 0.f, glp = 0.f;
+        int y = -1;
+        if (row_ok) {
+          const int cr = p.chunk_start + row;
+          lse2 = p.lse_c[cr] * kLog2e;
+          glp = p.glp_c[cr];
+          y = p.targets_c[cr];
+          if (p.gent_c != nullptr) {
+            const float ge = p.gent_c[cr];
+            ca = ge * kLn2;
+            cb = glp + ge * p.ent_c[cr];
+          } else {
+            cb = glp;
+          }
+        }
+        __nv_bfloat16* drow = p.dz + static_cast<int64_t>(row) * p.dz_ld;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait();
+          if (c == kBN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+          const int col = col_tile + c * 32;
+          if (col >= p.V) continue;
+          uint32_t packed[16];
+          if (row_ok) {
+            float g[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float d = fmaf(__uint_as_float(r[j]), kLog2e, -lse2);
+              const float pe = fast_exp2(d);
+              g[j] = -pe * fmaf(ca, d, cb);
+            }
+            if (static_cast<unsigned>(y - col) < 32u) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == y - col) g[j] += glp;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) packed[j] = 0u;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(drow + col);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            if (col + 8 * v < p.V)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+        }
+      } else if (MODE == kDh) {
+        const int row = mt * kBM + row_local;
+        const bool row_ok = row < rows_valid;
+        const int64_t orow = row_ok ? p.idx[p.chunk_start + row] : 0;
+        __nv_bfloat16* hrow = p.dhidden + orow * p.H;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait();
+          if (c == kBN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+          const int col = col_tile + c * 32;
+          if (!row_ok || col >= p.H) continue;
+          uint4* dst = reinterpret_cast<uint4*>(hrow + col);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            if (col + 8 * v < p.H) {
+              dst[v] = make_uint4(
+                  pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                  pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                  pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                  pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+            }
+          }
+        }
+      } else {  // kDw
+        const int vrow = mt * kBM + row_local;
+        const bool row_ok = vrow < p.V;
+        float* wrow = p.dw + static_cast<int64_t>(row_ok ? vrow : 0) * p.H;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          if (num_kb > 0) {
+            __syncwarp();
+          tmem_ld32(tbase + c * 32, r);
+            tmem_ld_wait();
+            if (c == kBN / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(&tempty[acc]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          const int col = col_tile + c * 32;
+          if (!row_ok || col >= p.H) continue;
+          float4* dst = reinterpret_cast<float4*>(wrow + col);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            if (col + 4 * v < p.H) {
+              float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+              if (p.beta) {
+                const float4 old = dst[v];
+                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+              }
+              dst[v] = o;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
+                           const TcGemmParams& p, int grid, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  tc_gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(tma_a, tma_b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace lmhead

@@ -1,0 +1,261 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Integer work (keep mask, compaction, Nk) must match bit for bit; logprob,
+entropy and lse within 1e-3 absolute; dhidden and dW within 1e-2 relative
+Frobenius error (bf16 inputs, fp32 accumulation, bf16 logit gradient).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import lmhead_oracle as O
+from sft_keep_mask_gb300 import lmhead as L
+from sft_keep_mask_gb300 import synth
+from sft_keep_mask_gb300.api import LMHeadScorer
+from tests._util import (assert_frob_close, assert_rows_close, gpu_keep, oracle_keep,
+                         seq_offsets, to64)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _run_both(w, chunk_rows=0, want_entropy=True, grad_entropy=True, keep_override="auto",
+              accumulate=False, check_bwd=True):
+    inp = synth.make_inputs(w, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=chunk_rows)
+    if keep_override == "auto":
+        keep = gpu_keep(sc, inp)
+        keep_np = oracle_keep(inp)
+        np.testing.assert_array_equal(keep.cpu().numpy(), keep_np)
+    elif keep_override is None:
+        keep, keep_np = None, None
+    else:
+        keep_np = keep_override
+        keep = torch.from_numpy(keep_np).to(DEV)
+    g_ent = inp["grad_entropy"] if grad_entropy else None
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep, want_entropy)
+    out = dict(lp=lp, ent=ent, lse=lse)
+    if check_bwd:
+        dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                             inp["grad_logprob"], g_ent, accumulate=accumulate)
+        out.update(dh=dh, dW=dW)
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+
+    h, W = to64(inp["hidden"]), to64(inp["weight"])
+    y = inp["targets"].cpu().numpy()
+    olp, oent, olse = O.forward(h, W, y, keep_np, want_entropy)
+    assert_rows_close(lp.cpu().double().numpy(), olp, "logprob")
+    assert_rows_close(lse.cpu().double().numpy(), olse, "lse")
+    if want_entropy:
+        assert_rows_close(ent.cpu().double().numpy(), oent, "entropy")
+    skipped = np.zeros(w.N, bool) if keep_np is None else keep_np == 0
+    assert (lp.cpu().numpy()[skipped] == 0).all() and (lse.cpu().numpy()[skipped] == 0).all()
+    if check_bwd:
+        odh, odW = O.backward(h, W, y, keep_np, inp["grad_logprob"].cpu().double().numpy(),
+                              None if g_ent is None else g_ent.cpu().double().numpy())
+        assert_frob_close(to64(out["dh"]), odh, "dhidden")
+        assert_frob_close(out["dW"].cpu().double().numpy(), odW, "dW")
+        assert (out["dh"].cpu()[torch.from_numpy(skipped)] == 0).all()
+    return inp, keep, keep_np, out, sc
+
+
+def test_tiny_forward_backward_with_entropy_gradient():
+    _run_both(synth.workload("tiny"))
+
+
+def test_multi_tile_ragged_multi_chunk():
+    # N, H, V not multiples of the tiles; 4 chunks of 256 kept rows; packed
+    # sequences build the keep mask on the device
+    w = synth.workload("moe30b_rl", N=3000, H=384, V=5000)
+    _run_both(w, chunk_rows=256)
+
+
+def test_metric_only_entropy_and_no_entropy():
+    w = synth.workload("tiny", seed=7, N=700, H=192, V=3000)
+    _run_both(w, want_entropy=True, grad_entropy=False)
+    _run_both(w, want_entropy=False, grad_entropy=False)
+
+
+def test_keep_none_scores_every_row():
+    w = synth.workload("tiny", seed=8, N=300, H=128, V=2100)
+    _run_both(w, keep_override=None)
+
+
+def test_empty_keep_mask():
+    w = synth.workload("tiny", seed=9, N=200, H=64, V=1000)
+    inp, keep, _, out, sc = _run_both(w, keep_override=np.zeros(200, np.uint8))
+    assert not out["lp"].any() and not out["lse"].any() and not out["ent"].any()
+    assert not out["dh"].any() and not out["dW"].any()
+    # with accumulation the weight gradient is left as it was
+    dW = torch.full((w.V, w.H), 3.0, device=DEV)
+    sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, out["lse"], out["ent"],
+                inp["grad_logprob"], inp["grad_entropy"], dweight=dW, accumulate=True)
+    torch.cuda.synchronize()
+    assert (dW == 3.0).all()
+
+
+def test_single_kept_row_and_vocab_tail():
+    w = synth.workload("tiny", seed=10, N=64, H=64, V=257)
+    keep = np.zeros(64, np.uint8)
+    keep[37] = 1
+    _run_both(w, keep_override=keep)
+
+
+def test_gradient_accumulation_and_determinism():
+    w = synth.workload("tiny", seed=11, N=640, H=256, V=4100)
+    inp = synth.make_inputs(w, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
+    keep = inp["keep"]
+    args = (inp["hidden"], inp["weight"], inp["targets"], keep)
+    lp1, ent1, lse1 = sc.forward(*args)
+    lp2, ent2, lse2 = sc.forward(*args)
+    assert torch.equal(lp1, lp2) and torch.equal(ent1, ent2) and torch.equal(lse1, lse2)
+    g = (inp["grad_logprob"], inp["grad_entropy"])
+    dh1, dW1 = sc.backward(*args, lse1, ent1, *g)
+    dh2, dW2 = sc.backward(*args, lse1, ent1, *g)
+    assert torch.equal(dh1, dh2) and torch.equal(dW1, dW2)
+    sc.backward(*args, lse1, ent1, *g, dweight=dW2, accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.allclose(dW2, 2 * dW1, rtol=1e-6, atol=1e-7)
+
+
+def test_peaked_rows():
+    w = synth.workload("tiny", seed=12, N=300, H=256, V=4096, w_scale=16.0)
+    inp, _, _, out, _ = _run_both(w)
+    lp = out["lp"].cpu().numpy()
+    assert (lp <= 1e-5).all()
+
+
+def test_compaction_and_expand_bit_exact():
+    rng = np.random.default_rng(13)
+    for n in (1, 255, 4096, 4097, 20000):
+        keep_np = (rng.random(n) < 0.37).astype(np.uint8)
+        y = torch.from_numpy(rng.integers(0, 50, n)).to(DEV)
+        sc = LMHeadScorer(n, 64, 50)
+        idx, yc, nk = sc.compact(torch.from_numpy(keep_np).to(DEV), y)
+        oidx, onk, oyc = O.compact(keep_np, y.cpu().numpy(), 50)
+        assert int(nk.item()) == onk
+        np.testing.assert_array_equal(idx[:onk].cpu().numpy(), oidx)
+        np.testing.assert_array_equal(yc[:onk].cpu().numpy(), oyc)
+        src = torch.arange(n, dtype=torch.float32, device=DEV) + 1
+        dst = torch.full((n,), 7.0, device=DEV)
+        L.lmhead_expand(src, idx, nk, n, dst)
+        want = np.zeros(n, np.float32)
+        want[oidx] = np.arange(onk, dtype=np.float32) + 1
+        np.testing.assert_array_equal(dst.cpu().numpy(), want)
+
+
+def test_keep_mask_builder_bit_exact():
+    rng = np.random.default_rng(14)
+    lens = [int(x) for x in rng.integers(1, 300, 40)]
+    n = sum(lens)
+    comps = [((rng.random(n) < p) * rng.standard_normal(n)).astype(np.float32)
+             for p in (0.3, 0.1, 0.05)]
+    sc = LMHeadScorer(n, 64, 50)
+    t = [torch.from_numpy(c).to(DEV) for c in comps]
+    for k in range(1, 4):
+        keep = sc.keep_mask(*(t[:k] + [None] * (3 - k)), seq_lens=lens)
+        np.testing.assert_array_equal(keep.cpu().numpy(), O.build_keep_mask(comps[:k], lens))
+
+
+def test_target_out_of_range_sets_status():
+    w = synth.workload("tiny", seed=15, N=128, H=64, V=500)
+    inp = synth.make_inputs(w, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    keep = torch.zeros(w.N, dtype=torch.uint8, device=DEV)
+    keep[5] = 1
+    y = inp["targets"].clone()
+    y[6] = -100          # skipped row: never read
+    sc.forward(inp["hidden"], inp["weight"], y, keep)
+    assert sc.status() == 0
+    y[5] = w.V           # kept row out of range
+    sc.forward(inp["hidden"], inp["weight"], y, keep)
+    assert sc.status() == L.LMHEAD_ETARGET
+
+
+def test_no_allocation_inside_calls():
+    w = synth.workload("tiny", seed=16, N=512, H=256, V=4096)
+    inp = synth.make_inputs(w, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    lp = torch.empty(w.N, device=DEV)
+    ent = torch.empty(w.N, device=DEV)
+    lse = torch.empty(w.N, device=DEV)
+    dh = torch.empty_like(inp["hidden"])
+    dW = torch.empty(w.V, w.H, device=DEV)
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"], out=(lp, ent, lse))
+    sc.backward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"], lse, ent,
+                inp["grad_logprob"], inp["grad_entropy"], dweight=dW, dhidden=dh)
+    torch.cuda.synchronize()
+    assert torch.cuda.max_memory_allocated() == base
+
+
+# ------------------------------------------------------------ full sizes
+
+def _sampled_rows_check(w, inp, keep, out, count, with_bwd):
+    """Oracle on sampled kept rows (row-local outputs) of a full-size batch."""
+    kept = torch.nonzero(keep).flatten().cpu().numpy() if keep is not None else np.arange(w.N)
+    pick = kept[synth.sample_rows(len(kept), count, w.seed)]
+    rows = torch.from_numpy(pick).to(DEV)
+    W = to64(inp["weight"])
+    h = to64(inp["hidden"][rows])
+    y = inp["targets"][rows].cpu().numpy()
+    g1 = inp["grad_logprob"][rows].cpu().double().numpy() if with_bwd else None
+    g2 = (inp["grad_entropy"][rows].cpu().double().numpy()
+          if with_bwd and inp["grad_entropy"] is not None else None)
+    lp, ent, lse, dh, _ = O.score_rows(h, W, y, g1, g2)
+    assert_rows_close(out["lp"][rows].cpu().double().numpy(), lp, "logprob (sampled)")
+    assert_rows_close(out["ent"][rows].cpu().double().numpy(), ent, "entropy (sampled)")
+    assert_rows_close(out["lse"][rows].cpu().double().numpy(), lse, "lse (sampled)")
+    if with_bwd:
+        assert_frob_close(to64(out["dh"][rows]), dh, "dhidden (sampled rows)")
+
+
+def test_full_size_qwen3_4b_forward_sampled():
+    w = synth.workload("qwen3_4b")
+    inp = synth.make_inputs(w, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    keep = gpu_keep(sc, inp)
+    np.testing.assert_array_equal(keep.cpu().numpy(), oracle_keep(inp))
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    k = keep.bool()
+    assert (lp[k] <= 1e-5).all()
+    assert (ent[k] >= -1e-5).all() and (ent[k] <= math.log(w.V) + 1e-4).all()
+    assert (lp[~k] == 0).all() and (ent[~k] == 0).all()
+    _sampled_rows_check(w, inp, keep, dict(lp=lp, ent=ent, lse=lse), 48, False)
+
+
+def test_full_size_moe30b_rl_forward_backward_sampled():
+    w = synth.workload("moe30b_rl")
+    inp = synth.make_inputs(w, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    keep = gpu_keep(sc, inp)
+    np.testing.assert_array_equal(keep.cpu().numpy(), oracle_keep(inp))
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+    dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                         inp["grad_logprob"], inp["grad_entropy"])
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    _sampled_rows_check(w, inp, keep, dict(lp=lp, ent=ent, lse=lse, dh=dh), 24, True)
+    k = keep.bool()
+    assert (dh[~k] == 0).all()
+    # every row's logit gradient sums to zero over the vocabulary, so the
+    # columns of dW sum to (nearly) zero
+    col = dW.double().sum(0)
+    assert col.abs().max().item() <= 1e-3 * dW.double().abs().sum(0).max().item()
+
+
+def test_full_vocab_slice_weight_gradient():
+    # full H and V, a 192-row slice: the oracle computes the whole dW
+    w = synth.workload("moe30b_rl", N=192)
+    keep_np = (np.random.default_rng(17).random(w.N) < 0.5).astype(np.uint8)
+    _run_both(w, keep_override=keep_np, chunk_rows=64)
