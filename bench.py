@@ -125,6 +125,16 @@ def cpu_oracle_rate(inp, keep_np, W64, rows):
     return rows / dt, dt
 
 
+def _workload(args):
+    from sft_keep_mask_gb300 import synth
+    over = {}
+    if args.rows:
+        over["N"] = args.rows
+    if args.vocab:
+        over["V"] = args.vocab
+    return synth.workload(args.workload, **over)
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -141,7 +151,7 @@ def run_reference(args):
     import torch
     from oracle import lmhead_oracle as O
     from sft_keep_mask_gb300 import synth
-    w = synth.workload(args.workload)
+    w = _workload(args)
     inp = synth.make_inputs(w, device="cpu")
     keep = O.build_keep_mask([c.numpy() for c in inp["components"]], inp["seq_lens"]) \
         if "components" in inp else inp["keep"].numpy()
@@ -189,8 +199,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     L.lib()
 
-    w = synth.workload(args.workload)
-    w = synth.workload(args.workload, seed=w.seed + 100 * rank)
+    w = _workload(args)
+    w = synth.workload(args.workload, N=w.N, V=w.V, seed=w.seed + 100 * rank)
     inp = synth.make_inputs(w, device=dev)
     sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=args.chunk_rows, device=dev)
     comps = inp.get("components")
@@ -365,6 +375,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="moe30b_rl")
     ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0, help="override N (profiling cases)")
+    ap.add_argument("--vocab", type=int, default=0, help="override V (profiling cases)")
     ap.add_argument("--entropy-grad", type=int, default=1)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")

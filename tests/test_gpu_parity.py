@@ -27,7 +27,7 @@ def _run_both(w, chunk_rows=0, want_entropy=True, grad_entropy=True, keep_overri
               accumulate=False, check_bwd=True):
     inp = synth.make_inputs(w, device=DEV)
     sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=chunk_rows)
-    if keep_override == "auto":
+    if isinstance(keep_override, str):
         keep = gpu_keep(sc, inp)
         keep_np = oracle_keep(inp)
         np.testing.assert_array_equal(keep.cpu().numpy(), keep_np)
