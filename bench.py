@@ -61,6 +61,9 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        import threading
+        self.lines = []
+        first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -68,20 +71,30 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+            return self
+
+        def reader():
+            for ln in self.proc.stdout:
+                if ln.strip():
+                    self.lines.append(ln)
+                    first.set()
+            first.set()
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        # the timed region starts only once the sampler is up and sampling
+        first.wait(timeout=15.0)
         return self
 
     def __exit__(self, *a):
-        self.lines = []
         if self.proc is not None:
-            time.sleep(0.2)
+            time.sleep(0.15)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out = ""
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            self.thread.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -261,6 +274,9 @@ def run_ours(args):
         barrier()
     L.lmhead_profile_enable(False)
     launches = L.lmhead_launch_count() - launches0
+    status_timed = L.lmhead_get_status(ws)
+    if status_timed != 0:
+        raise RuntimeError(f"device status {status_timed} after the timed steps")
     prof = L.lmhead_profile_read()
     ms = ev0.elapsed_time(ev1)
     if world > 1:
@@ -331,6 +347,8 @@ def run_ours(args):
             t = torch.tensor([el], device=dev, dtype=torch.float64)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             el = float(t[0])
+        if L.lmhead_get_status(ws) != 0:
+            raise RuntimeError("device status non-zero after the end-to-end steps")
         e2e = {"value": nk_total * args.steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * el / args.steps}
 
@@ -360,7 +378,8 @@ def run_ours(args):
             "frac_of_sustained_peak": tflops / sustained,
             "gemm_tflops": gemm_tflops,
             "roofline": roof, "kernels": kernels, "gpu_launches": launches,
-            "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+            "clocks": clk.summary(), "device_status": status_timed, "e2e": e2e,
+            "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

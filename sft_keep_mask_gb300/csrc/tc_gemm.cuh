@@ -48,11 +48,15 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
 }
 
 // Wait without the abort check: used only to drain copies / MMAs in flight
-// before the CTA releases its shared and tensor memory.
-__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+// before the CTA releases its shared and tensor memory.  Running out of time
+// here is recorded like any other timeout.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, 0, kStatusTimeout);
+      return;
+    }
   }
 }
 
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // Let every load that was issued land before the CTA exits.
       for (int s = 0; s < kStages; ++s) {
         const uint32_t uses = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
-        if (uses > 0) mbar_wait_drain(&full[s], (uses - 1u) & 1u);
+        if (uses > 0) mbar_wait_drain(&full[s], (uses - 1u) & 1u, p.status);
       }
     }
     __syncwarp();
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // No MMA may still be running when the accumulators are released.
       umma_commit(drain);
-      mbar_wait_drain(drain, 0);
+      mbar_wait_drain(drain, 0, p.status);
     }
     __syncwarp();
   } else {
