@@ -155,6 +155,41 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
                          lmhead_stream_t stream);
 
 /*
+ * Largest N accepted by lmhead_compact_noalloc (4096 scan blocks of 4096 rows).
+ */
+#define LMHEAD_NOALLOC_MAX_ROWS 16777216
+
+/*
+ * lmhead_compact_noalloc -- the same stable compaction as lmhead_compact, for
+ * callers that cannot allocate device memory.  (The pages have no counterpart
+ * of this entry point; it exists for such callers only.)
+ *
+ * Who needs it: code that has no device allocator of its own -- a plugin or
+ * hook running inside a framework whose caching allocator owns the GPU's
+ * memory, or a service that reserves all its memory at start-up and must not
+ * call cudaMalloc later (cudaMalloc can synchronise the device and can fail
+ * with out-of-memory mid-run).  Instead of a caller workspace, its scratch
+ * (the per-block kept-row counts, 16 KiB) is a fixed array inside the library
+ * that every GPU loading the library holds until the process exits.  The call
+ * performs no cudaMalloc/cudaFree and calls no allocating library routine.
+ *
+ *   keep, targets, N, V, idx, targets_c, d_nk : as for lmhead_compact.
+ *   d_status (out) : int32 [1] on the device; set to 0 by the call, then to
+ *                    LMHEAD_ETARGET if a kept row's target is outside [0, V).
+ *   Returns LMHEAD_EINVAL for N > LMHEAD_NOALLOC_MAX_ROWS (and for the
+ *   argument errors of lmhead_compact), LMHEAD_EUNSUPPORTED off sm_103.
+ *
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up per device, done with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array and
+ * it keeps the last call's contents: calls whose work overlaps on the GPU
+ * (e.g. on two streams at once) race and must be ordered by the caller.
+ */
+lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64_t* targets, int64_t N,
+                                     int V, int32_t* idx, int32_t* targets_c, int32_t* d_nk,
+                                     int32_t* d_status, lmhead_stream_t stream);
+
+/*
  * Expand compacted per-row values back to all rows ([P1] Overview: expand
  * back, skipped positions get zeros).
  *   src  : float32 [Nk]   idx : int32 [Nk] (from lmhead_compact)

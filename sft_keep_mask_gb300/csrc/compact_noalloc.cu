@@ -1,0 +1,97 @@
+// lmhead_compact_noalloc: the stable compaction of lmhead_compact for callers
+// that cannot hand the library a workspace.
+//
+// Some callers have no way to obtain device memory of their own: a plugin or
+// hook that runs inside a host framework whose caching allocator owns all of
+// the GPU's memory, or a long-running service that reserves its memory at
+// start-up and must not allocate afterwards (cudaMalloc may synchronise the
+// device and can fail with out-of-memory in the middle of a run).  For them
+// this entry point keeps its scratch -- the per-block counts of kept rows --
+// in a fixed array that is part of the library image on every GPU that loads
+// it, so the caller passes only its inputs and outputs.
+//
+// The scratch is shared by every call on a device and keeps the last call's
+// contents.  Each call writes every count it later reads before reading it,
+// so nothing has to start at zero; the one value that must (the device status
+// word) is a caller output and is cleared by each call.  Two calls whose work
+// overlaps on the GPU (different streams, or different host threads on one
+// stream without ordering) race on the shared array: order them.
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/lmhead.h"
+#include "internal.h"
+
+namespace lmhead {
+namespace {
+
+constexpr int kNoallocRowsPerBlock = kCompactRowsPerBlock;  // rows per scan block
+constexpr int kNoallocMaxBlocks =
+    static_cast<int>(LMHEAD_NOALLOC_MAX_ROWS / kNoallocRowsPerBlock);  // 4096 counts = 16 KiB
+
+static_assert(LMHEAD_NOALLOC_MAX_ROWS % kNoallocRowsPerBlock == 0,
+              "maximum rows must be a whole number of scan blocks");
+
+// Per-block kept-row counts of the compaction scan (the only scratch).
+static __device__ __align__(256) int32_t g_noalloc_counts[kNoallocMaxBlocks];
+
+// Device address of g_noalloc_counts, looked up once per device.
+struct ScratchAddr {
+  int32_t* ptr = nullptr;
+  bool ready = false;
+};
+constexpr int kMaxDevices = 64;
+ScratchAddr g_scratch[kMaxDevices];
+std::mutex g_scratch_mu;
+
+lmhead_status scratch_for_current_device(int32_t** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return LMHEAD_ECUDA;
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  if (!g_scratch[dev].ready) {
+    void* p = nullptr;
+    // In host code g_noalloc_counts names a host-side shadow, not device
+    // memory; the device address must come from the runtime.
+    if (cudaGetSymbolAddress(&p, g_noalloc_counts) != cudaSuccess || p == nullptr)
+      return LMHEAD_ECUDA;
+    g_scratch[dev].ptr = static_cast<int32_t*>(p);
+    g_scratch[dev].ready = true;
+  }
+  *out = g_scratch[dev].ptr;
+  return LMHEAD_OK;
+}
+
+}  // namespace
+}  // namespace lmhead
+
+extern "C" lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64_t* targets,
+                                                int64_t N, int V, int32_t* idx,
+                                                int32_t* targets_c, int32_t* d_nk,
+                                                int32_t* d_status, lmhead_stream_t stream) {
+  using namespace lmhead;
+  if (N < 0 || V < 1 || targets == nullptr || idx == nullptr || targets_c == nullptr ||
+      d_nk == nullptr || d_status == nullptr)
+    return LMHEAD_EINVAL;
+  if (N > LMHEAD_NOALLOC_MAX_ROWS) return LMHEAD_EINVAL;
+  int major = 0, minor = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      major != 10 || minor != 3)
+    return LMHEAD_EUNSUPPORTED;
+  int32_t* counts = nullptr;
+  lmhead_status st = scratch_for_current_device(&counts);
+  if (st != LMHEAD_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_status, 0, sizeof(int32_t), s) != cudaSuccess) return LMHEAD_ECUDA;
+  if (N == 0) {
+    return cudaMemsetAsync(d_nk, 0, sizeof(int32_t), s) == cudaSuccess ? LMHEAD_OK
+                                                                        : LMHEAD_ECUDA;
+  }
+  if (launch_compact(keep, targets, N, V, idx, targets_c, d_nk, counts, d_status, s) !=
+      cudaSuccess)
+    return LMHEAD_ECUDA;
+  return LMHEAD_OK;
+}

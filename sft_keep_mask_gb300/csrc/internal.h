@@ -54,6 +54,9 @@ template <int MODE>
 cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                            const TcGemmParams& p, int grid, cudaStream_t stream);
 
+// Rows counted by one block of the compaction scan (rowops.cu).
+constexpr int kCompactRowsPerBlock = 4096;
+
 // Row kernels (rowops.cu).
 cudaError_t launch_build_keep(const float* c0, const float* c1, const float* c2,
                               const int32_t* offsets, int n_seq, int64_t N, uint8_t* keep,

@@ -20,6 +20,7 @@ namespace {
 constexpr int kScanThreads = 256;
 constexpr int kScanPerThread = 16;
 constexpr int kScanTile = kScanThreads * kScanPerThread;  // rows per block
+static_assert(kScanTile == kCompactRowsPerBlock, "scan block size");
 
 // ---------------------------------------------------------------- keep mask
 __global__ void build_keep_kernel(const float* __restrict__ c0, const float* __restrict__ c1,
