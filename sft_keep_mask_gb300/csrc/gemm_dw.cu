@@ -1,8 +1,12 @@
-// Instantiation of the tcgen05 GEMM for the kDw contraction (one
-// translation unit per contraction so the four compile in parallel).
+// Instantiations of the tcgen05 GEMMs (one-CTA and CTA-pair) for the kDw
+// contraction; one translation unit per contraction so the four compile in
+// parallel.
 #include "tc_gemm.cuh"
+#include "tc_gemm2.cuh"
 
 namespace lmhead {
 template cudaError_t launch_tc_gemm<kDw>(const CUtensorMap&, const CUtensorMap&,
                                            const TcGemmParams&, int, cudaStream_t);
+template cudaError_t launch_tc_gemm_pair<kDw>(const CUtensorMap&, const CUtensorMap&,
+                                                const TcGemmParams&, int, cudaStream_t);
 }  // namespace lmhead

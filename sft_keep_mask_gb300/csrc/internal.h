@@ -54,6 +54,12 @@ template <int MODE>
 cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                            const TcGemmParams& p, int grid, cudaStream_t stream);
 
+// The same contractions on CTA pairs (256 x 256 tiles, cta_group::2); `grid`
+// must be even.  Its B maps use 128-row boxes (each CTA stages half of B).
+template <int MODE>
+cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
+                                const TcGemmParams& p, int grid, cudaStream_t stream);
+
 // Rows counted by one block of the compaction scan (rowops.cu).
 constexpr int kCompactRowsPerBlock = 4096;
 

@@ -4,6 +4,7 @@
 // four tcgen05 GEMM instantiations).
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -16,6 +17,8 @@
 
 namespace lmhead {
 namespace {
+
+constexpr bool kDefaultPair = true;
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 inline int64_t cdiv(int64_t x, int64_t m) { return (x + m - 1) / m; }
@@ -221,6 +224,30 @@ int gemm_grid(int64_t tiles) {
   return static_cast<int>(tiles < sms ? (tiles < 1 ? 1 : tiles) : sms);
 }
 
+// GEMM variant: CTA pairs (256 x 256 tiles) unless LMHEAD_GEMM=single asks
+// for the one-CTA kernel (128 x 256 tiles).
+bool use_pair() {
+  const char* e = std::getenv("LMHEAD_GEMM");
+  if (e == nullptr) return kDefaultPair;
+  return std::strcmp(e, "single") != 0;
+}
+
+// Launches one contraction on the selected variant.  m_upper bounds the rows
+// of D (the chunk for kFwd/kDz/kDh, V for kDw); b_single / b_pair are the B
+// maps for the two variants (they differ only for K-major B).
+template <int MODE>
+cudaError_t run_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b_single,
+                     const CUtensorMap& b_pair, const TcGemmParams& p, int64_t m_upper,
+                     int64_t n, cudaStream_t s) {
+  if (pair) {
+    const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, kBN);
+    const int64_t pairs = device_info().sms / 2;
+    const int grid = static_cast<int>(2 * (tiles < pairs ? (tiles < 1 ? 1 : tiles) : pairs));
+    return launch_tc_gemm_pair<MODE>(a, b_pair, p, grid, s);
+  }
+  return launch_tc_gemm<MODE>(a, b_single, p, gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN)), s);
+}
+
 }  // namespace
 
 int device_sm_count() { return device_info().sms; }
@@ -301,9 +328,11 @@ lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* 
                    s);
   if (st != LMHEAD_OK) return st;
 
-  CUtensorMap ma, mb;
+  const bool pair = use_pair();
+  CUtensorMap ma, mb, mb2;
   if (!make_map(&ma, hc, L.C, H, H, kBM, 64) ||
-      !make_map(&mb, weight, V, H, H, kBN, 64))
+      !make_map(&mb, weight, V, H, H, kBN, 64) ||
+      !make_map(&mb2, weight, V, H, H, 128, 64))
     return LMHEAD_ECUDA;
 
   TcGemmParams p{};
@@ -316,7 +345,6 @@ lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* 
   p.targets_c = yc;
   p.want_entropy = want_entropy ? 1 : 0;
   p.part = part;
-  const int grid = gemm_grid(cdiv(L.C, kBM) * L.num_vt);
 
   for (int64_t cs = 0; cs < N; cs += L.C) {
     {
@@ -327,7 +355,7 @@ lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* 
     p.chunk_start = static_cast<int>(cs);
     {
       Launch l(kKindGemmFwd, s);
-      LM_TRY(launch_tc_gemm<kFwd>(ma, mb, p, grid, s));
+      LM_TRY(run_gemm<kFwd>(pair, ma, mb, mb2, p, L.C, V, s));
     }
     {
       Launch l(kKindMerge, s);
@@ -393,9 +421,11 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
     LM_TRY(launch_zero_skipped_rows(keep, N, H, static_cast<__nv_bfloat16*>(dhidden), s));
   }
 
-  CUtensorMap m_hc_k, m_w_k, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn;
+  const bool pair = use_pair();
+  CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn;
   if (!make_map(&m_hc_k, hc, L.C, H, H, kBM, 64) ||        // A of kDz (K-major)
       !make_map(&m_w_k, weight, V, H, H, kBN, 64) ||       // B of kDz (K-major)
+      !make_map(&m_w_k2, weight, V, H, H, 128, 64) ||      // B of kDz, CTA pairs
       !make_map(&m_dz_k, dz, L.C, V, L.dz_ld, kBM, 64) ||  // A of kDh (K-major)
       !make_map(&m_w_mn, weight, V, H, H, 64, 64) ||       // B of kDh (MN-major boxes)
       !make_map(&m_dz_mn, dz, L.C, V, L.dz_ld, 64, 64) ||  // A of kDw (MN-major boxes)
@@ -420,9 +450,6 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
   p.dhidden = static_cast<__nv_bfloat16*>(dhidden);
   p.dw = dweight;
   const int64_t n_h_tiles = cdiv(H, kBN);
-  const int grid_dz = gemm_grid(cdiv(L.C, kBM) * L.num_vt);
-  const int grid_dh = gemm_grid(cdiv(L.C, kBM) * n_h_tiles);
-  const int grid_dw = gemm_grid(cdiv(V, kBM) * n_h_tiles);
 
   for (int64_t cs = 0; cs < N; cs += L.C) {
     p.chunk_start = static_cast<int>(cs);
@@ -434,18 +461,18 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
     {
       Launch l(kKindGemmDz, s);
       p.group_n = 16;
-      LM_TRY(launch_tc_gemm<kDz>(m_hc_k, m_w_k, p, grid_dz, s));
+      LM_TRY(run_gemm<kDz>(pair, m_hc_k, m_w_k, m_w_k2, p, L.C, V, s));
     }
     {
       Launch l(kKindGemmDh, s);
       p.group_n = static_cast<int>(n_h_tiles);
-      LM_TRY(launch_tc_gemm<kDh>(m_dz_k, m_w_mn, p, grid_dh, s));
+      LM_TRY(run_gemm<kDh>(pair, m_dz_k, m_w_mn, m_w_mn, p, L.C, H, s));
     }
     {
       Launch l(kKindGemmDw, s);
       p.group_n = static_cast<int>(n_h_tiles);
       p.beta = (cs > 0 || dw_accumulate) ? 1 : 0;
-      LM_TRY(launch_tc_gemm<kDw>(m_dz_mn, m_hc_mn, p, grid_dw, s));
+      LM_TRY(run_gemm<kDw>(pair, m_dz_mn, m_hc_mn, m_hc_mn, p, V, H, s));
     }
   }
   return LMHEAD_OK;

@@ -1,0 +1,272 @@
+// Pieces shared by the one-CTA and the CTA-pair tcgen05 GEMMs: the tile
+// raster, the drain wait and the fused epilogues of the four contractions.
+//
+// The epilogues read one accumulator row per thread (TMEM lane = row) in
+// slices of 32 fp32 columns:
+//   kFwd  per-row online softmax over the 256-column vocab tile: running max
+//         m (log2 units), s = sum 2^(z2 - m), u = sum 2^(z2 - m) (z2 - m), and
+//         the target logit; written as (m ln2, s, u ln2, t) partials.  This is
+//         the single fused projection for log-prob and entropy of SkyRL pull
+//         request #2374 ("How it works"), with the entropy -(p log p) of its
+//         gemini-code-assist review kept in max-shifted form.
+//   kDz   dz = g_lp (1[v=y] - p) - g_ent p (log p + H) from the recomputed
+//         logit, p = exp(z - lse) (the backward of the same page; logits
+//         recomputed rather than saved, twinkle pull request #283, section 1),
+//         stored as bf16.
+//   kDh   bf16 rows scattered to dhidden[idx[row]].
+//   kDw   fp32 dW tile, written or added to.
+#pragma once
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lmhead {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Tile t -> (row tile, column tile).  Tiles walk `group_n` column tiles for
+// every row tile before the next group, so the CTAs in flight share the
+// group's column operand through L2.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_n, int& mt,
+                                            int& nt) {
+  const int per_group = num_m * group_n;
+  const int g = t / per_group;
+  const int local = t - g * per_group;
+  const int rem = num_n - g * group_n;
+  const int gn = rem < group_n ? rem : group_n;
+  mt = local / gn;
+  nt = g * group_n + (local - (local / gn) * gn);
+}
+
+// Wait without the abort check: used only to drain copies / MMAs in flight
+// before the CTA releases its shared and tensor memory.  Running out of time
+// here is recorded like any other timeout.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, 0, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+// Epilogue of one 256-column accumulator tile for this thread's row.
+//   tbase      TMEM address of (this warp's lane quarter, column 0 of the tile)
+//   row        kFwd/kDz/kDh: row within the chunk; kDw: vocabulary row
+//   nt         column tile
+//   rows_valid rows of the chunk that hold kept tokens
+//   have_acc   false only for kDw with an empty K range (writes zeros)
+//   release    called once, right after the last TMEM load of the tile
+template <int MODE, typename Release>
+__device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tbase, int row,
+                                              int nt, int rows_valid, bool have_acc,
+                                              Release&& release) {
+  constexpr int kSlices = kBN / 32;
+  const int col_tile = nt * kBN;
+
+  if (MODE == kFwd) {
+    const bool row_ok = row < rows_valid;
+    const int y = row_ok ? p.targets_c[p.chunk_start + row] : -1;
+    const bool tail = col_tile + kBN > p.V;
+    float m2 = -INFINITY, s = 0.f, u2 = 0.f, tz = -INFINITY;
+#pragma unroll 1
+    for (int c = 0; c < kSlices; ++c) {
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait();
+      if (c == kSlices - 1) release();
+      const int col = col_tile + c * 32;
+      float z[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]);
+      if (tail) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col + j >= p.V) z[j] = -INFINITY;
+      }
+      if (static_cast<unsigned>(y - col) < 32u) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == y - col) tz = z[j];
+      }
+      float cmax = z[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, z[j]);
+      if (cmax == -INFINITY) continue;  // slice wholly past the vocabulary
+      const float cm2 = cmax * kLog2e;
+      if (cm2 > m2) {
+        if (m2 != -INFINITY) {
+          const float sc = fast_exp2(m2 - cm2);
+          u2 = sc * (u2 + s * (m2 - cm2));
+          s *= sc;
+        }
+        m2 = cm2;
+      }
+      if (!tail) {
+        if (p.want_entropy) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float d = fmaf(z[j], kLog2e, -m2);
+            const float e = fast_exp2(d);
+            s += e;
+            u2 = fmaf(e, d, u2);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s += fast_exp2(fmaf(z[j], kLog2e, -m2));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (col + j < p.V) {
+            const float d = fmaf(z[j], kLog2e, -m2);
+            const float e = fast_exp2(d);
+            s += e;
+            u2 = fmaf(e, d, u2);
+          }
+        }
+      }
+    }
+    if (row_ok)
+      p.part[static_cast<int64_t>(nt) * p.chunk_rows + row] =
+          make_float4(m2 * kLn2, s, u2 * kLn2, tz);
+  } else if (MODE == kDz) {
+    const bool row_ok = row < rows_valid;
+    float lse2 = 0.f, ca = 0.f, cb = 0.f, glp = 0.f;
+    int y = -1;
+    if (row_ok) {
+      const int cr = p.chunk_start + row;
+      lse2 = p.lse_c[cr] * kLog2e;
+      glp = p.glp_c[cr];
+      y = p.targets_c[cr];
+      if (p.gent_c != nullptr) {
+        const float ge = p.gent_c[cr];
+        ca = ge * kLn2;
+        cb = glp + ge * p.ent_c[cr];
+      } else {
+        cb = glp;
+      }
+    }
+    __nv_bfloat16* drow = p.dz + static_cast<int64_t>(row) * p.dz_ld;
+#pragma unroll 1
+    for (int c = 0; c < kSlices; ++c) {
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait();
+      if (c == kSlices - 1) release();
+      const int col = col_tile + c * 32;
+      if (col >= p.V) continue;
+      uint32_t packed[16];
+      if (row_ok) {
+        float g[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float d = fmaf(__uint_as_float(r[j]), kLog2e, -lse2);
+          const float pe = fast_exp2(d);
+          g[j] = -pe * fmaf(ca, d, cb);
+        }
+        if (static_cast<unsigned>(y - col) < 32u) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == y - col) g[j] += glp;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) packed[j] = 0u;
+      }
+      uint4* dst = reinterpret_cast<uint4*>(drow + col);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        if (col + 8 * v < p.V)
+          dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                              packed[4 * v + 3]);
+    }
+  } else if (MODE == kDh) {
+    const bool row_ok = row < rows_valid;
+    const int64_t orow = row_ok ? p.idx[p.chunk_start + row] : 0;
+    __nv_bfloat16* hrow = p.dhidden + orow * p.H;
+#pragma unroll 1
+    for (int c = 0; c < kSlices; ++c) {
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait();
+      if (c == kSlices - 1) release();
+      const int col = col_tile + c * 32;
+      if (!row_ok || col >= p.H) continue;
+      uint4* dst = reinterpret_cast<uint4*>(hrow + col);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        if (col + 8 * v < p.H) {
+          dst[v] = make_uint4(
+              pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+              pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+              pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+              pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+        }
+      }
+    }
+  } else {  // kDw
+    const bool row_ok = row < p.V;
+    float* wrow = p.dw + static_cast<int64_t>(row_ok ? row : 0) * p.H;
+#pragma unroll 1
+    for (int c = 0; c < kSlices; ++c) {
+      uint32_t r[32];
+      if (have_acc) {
+        __syncwarp();
+        tmem_ld32(tbase + c * 32, r);
+        tmem_ld_wait();
+        if (c == kSlices - 1) release();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = 0u;
+      }
+      const int col = col_tile + c * 32;
+      if (!row_ok || col >= p.H) continue;
+      float4* dst = reinterpret_cast<float4*>(wrow + col);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        if (col + 4 * v < p.H) {
+          float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          if (p.beta) {
+            const float4 old = dst[v];
+            o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+          }
+          dst[v] = o;
+        }
+      }
+    }
+  }
+}
+
+// Problem extents of a contraction for this chunk (the number of kept rows
+// lives on the device).  Returns false when the launch has nothing to do.
+template <int MODE>
+__device__ __forceinline__ bool gemm_extents(const TcGemmParams& p, int& rows_valid, int& M,
+                                             int& N, int& K) {
+  const int nk = *p.d_nk;
+  rows_valid = nk - p.chunk_start;
+  rows_valid = rows_valid < 0 ? 0 : (rows_valid > p.chunk_rows ? p.chunk_rows : rows_valid);
+  if (MODE == kDw) {
+    M = p.V; N = p.H; K = rows_valid;
+    // An empty first chunk still has to clear dW when it is not accumulated.
+    return !(rows_valid == 0 && (p.beta || p.chunk_start > 0));
+  }
+  if (MODE == kDh) {
+    M = rows_valid; N = p.H; K = p.V;
+  } else {
+    M = rows_valid; N = p.V; K = p.H;
+  }
+  return rows_valid > 0;
+}
+
+}  // namespace lmhead

@@ -1,0 +1,226 @@
+// Persistent tcgen05 GEMM over CTA pairs (clusters of two CTAs on two SMs).
+//
+// Same contraction and epilogues as the one-CTA kernel (tc_gemm.cuh), with
+// 256 x 256 tiles computed by `tcgen05.mma.cta_group::2`: each CTA of the pair
+// stages its 128-row half of A and its 128-row half of B, the even CTA issues
+// the MMAs for both, and each CTA's tensor memory receives its 128 accumulator
+// rows (all 256 columns).  Per CTA a K step stages 32 KB instead of 48 KB, so
+// six stages fit and every operand byte fetched from L2 feeds twice the FLOPs.
+//
+//   warp 0      TMA producer of this CTA's halves; both CTAs count the bytes
+//               on the even CTA's full barrier
+//   warp 1      TMEM allocation (both CTAs, collectively) and, in the even
+//               CTA, the MMA issuer; commits are multicast to both CTAs
+//   warps 2..5  epilogue of this CTA's 128 rows; one elected lane per warp
+//               releases the accumulator on the even CTA's barrier
+#pragma once
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace lmhead {
+
+constexpr int kPairStages = 6;
+constexpr int kPairABytes = 128 * kBK * 2;   // this CTA's half of A
+constexpr int kPairBBytes = 128 * kBK * 2;   // this CTA's half of B
+constexpr int kPairSmemBytes = kPairStages * (kPairABytes + kPairBBytes) + 1024 + 256;
+constexpr int kPairTileM = 256;
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
+                        const __grid_constant__ CUtensorMap tma_b, const TcGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kPairStages * kPairABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPairStages * kPairBBytes);
+  uint64_t* empty = full + kPairStages;
+  uint64_t* tfull = empty + kPairStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+
+  int rows_valid, M, N, K;
+  if (!gemm_extents<MODE>(p, rows_valid, M, N, K)) return;  // uniform over the grid
+  const int num_m = (M + kPairTileM - 1) / kPairTileM;
+  const int num_n = (N + kBN - 1) / kBN;
+  const int num_kb = (K + kBK - 1) / kBK;
+  const int num_tiles = num_m * num_n;
+  if (pair >= num_tiles) return;  // both CTAs of the pair leave together
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // 4 epilogue warps in each CTA
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      const int half = static_cast<int>(rank) * 128;
+      for (int t = pair; t < num_tiles; t += num_pairs) {
+        int mt, nt;
+        tile_coords(t, num_m, num_n, p.group_n, mt, nt);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPairABytes + kPairBBytes));
+          const uint32_t bar = map_to_cta(smem_addr(&full[stage]), 0);
+          uint8_t* a_dst = sA + stage * kPairABytes;
+          uint8_t* b_dst = sB + stage * kPairBBytes;
+          const int k0 = kb * kBK;
+          const int m0 = mt * kPairTileM + half;
+          const int n0 = nt * kBN + half;
+          if (MODE == kDw) {
+            tma_load_2d_pair(a_dst, &tma_a, bar, m0, k0);
+            tma_load_2d_pair(a_dst + 8192, &tma_a, bar, m0 + 64, k0);
+          } else {
+            tma_load_2d_pair(a_dst, &tma_a, bar, k0, m0);
+          }
+          if (MODE == kDh || MODE == kDw) {
+            tma_load_2d_pair(b_dst, &tma_b, bar, n0, k0);
+            tma_load_2d_pair(b_dst + 8192, &tma_b, bar, n0 + 64, k0);
+          } else {
+            tma_load_2d_pair(b_dst, &tma_b, bar, k0, n0);
+          }
+          ++issued;
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // The even CTA sees every load of the pair complete on its full
+      // barriers; let them land before it exits.
+      if (leader) {
+        for (int s = 0; s < kPairStages; ++s) {
+          const uint32_t uses =
+              issued / kPairStages + (static_cast<uint32_t>(s) < issued % kPairStages ? 1u : 0u);
+          if (uses > 0) mbar_wait_drain(&full[s], (uses - 1u) & 1u, p.status);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      constexpr bool a_mn = (MODE == kDw);
+      constexpr bool b_mn = (MODE == kDh || MODE == kDw);
+      constexpr uint32_t idesc = idesc_bf16(kPairTileM, kBN, a_mn, b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok && num_kb > 0; t += num_pairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_addr(sA + stage * kPairABytes);
+          const uint32_t b_addr = smem_addr(sB + stage * kPairBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair(&empty[stage], 0x3);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[acc], 0x3);
+      }
+      umma_commit_pair(drain, 0x1);
+      mbar_wait_drain(drain, 0, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_local = static_cast<int>(rank) * 128 + q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int it = 0;
+    for (int t = pair; t < num_tiles; t += num_pairs, ++it) {
+      int mt, nt;
+      tile_coords(t, num_m, num_n, p.group_n, mt, nt);
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      if (num_kb > 0) {
+        if (!mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+      }
+      const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
+      const uint32_t te = map_to_cta(smem_addr(&tempty[acc]), 0);
+      epilogue_tile<MODE>(p, tbase, mt * kPairTileM + row_local, nt, rows_valid, num_kb > 0,
+                          [&] {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_cluster(te);
+                          });
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // the pair's MMAs and loads are finished in both CTAs
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
+                                const TcGemmParams& p, int grid, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPairSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  tc_gemm_pair_kernel<MODE><<<grid, kGemmThreads, kPairSmemBytes, stream>>>(tma_a, tma_b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace lmhead

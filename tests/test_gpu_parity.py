@@ -259,3 +259,51 @@ def test_full_vocab_slice_weight_gradient():
     w = synth.workload("moe30b_rl", N=192)
     keep_np = (np.random.default_rng(17).random(w.N) < 0.5).astype(np.uint8)
     _run_both(w, keep_override=keep_np, chunk_rows=64)
+
+
+# ------------------------------------------------------ one-CTA GEMM variant
+
+@pytest.fixture
+def single_cta(monkeypatch):
+    # the library reads LMHEAD_GEMM on every call; "single" selects the
+    # one-CTA tcgen05 kernel (128 x 256 tiles) instead of the CTA pairs
+    monkeypatch.setenv("LMHEAD_GEMM", "single")
+    yield
+
+
+def test_single_cta_variant_tiny(single_cta):
+    _run_both(synth.workload("tiny"))
+
+
+def test_single_cta_variant_ragged_multi_chunk(single_cta):
+    _run_both(synth.workload("moe30b_rl", N=3000, H=384, V=5000), chunk_rows=256)
+
+
+def test_single_cta_variant_empty_and_single_row(single_cta):
+    w = synth.workload("tiny", seed=10, N=64, H=64, V=257)
+    keep = np.zeros(64, np.uint8)
+    keep[37] = 1
+    _run_both(w, keep_override=keep)
+    _run_both(w, keep_override=np.zeros(64, np.uint8))
+
+
+def test_variants_agree_bitwise():
+    # the pair and one-CTA kernels accumulate every logit over K in the same
+    # order, so their outputs agree bit for bit
+    import os
+    w = synth.workload("tiny", seed=21, N=900, H=320, V=3000)
+    inp = synth.make_inputs(w, device=DEV)
+    res = []
+    for variant in ("pair", "single"):
+        os.environ["LMHEAD_GEMM"] = variant
+        try:
+            sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
+            lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
+            dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"], lse,
+                                 ent, inp["grad_logprob"], inp["grad_entropy"])
+            torch.cuda.synchronize()
+            res.append((lp, ent, lse, dh, dW))
+        finally:
+            del os.environ["LMHEAD_GEMM"]
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
