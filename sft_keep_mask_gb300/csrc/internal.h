@@ -33,6 +33,8 @@ struct TcGemmParams {
   int V;
   int H;
   int group_n;              // N tiles per raster group (L2 reuse)
+  int hint_a;               // L2 policy of A / B loads (CTA pairs): 0 none,
+  int hint_b;               //   1 evict first, 2 evict last, 3 evict normal
   int* status;              // device status word
   // epilogue operands (compact, indexed by compact row)
   const int32_t* targets_c;

@@ -94,6 +94,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       const int half = static_cast<int>(rank) * 128;
+      const uint64_t pol_a = make_l2_policy(p.hint_a);
+      const uint64_t pol_b = make_l2_policy(p.hint_b);
+      const bool ha = p.hint_a != 0, hb = p.hint_b != 0;
       for (int t = pair; t < num_tiles; t += num_pairs) {
         int mt, nt;
         tile_coords(t, num_m, num_n, p.group_n, mt, nt);
@@ -108,16 +111,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const int m0 = mt * kPairTileM + half;
           const int n0 = nt * kBN + half;
           if (MODE == kDw) {
-            tma_load_2d_pair(a_dst, &tma_a, bar, m0, k0);
-            tma_load_2d_pair(a_dst + 8192, &tma_a, bar, m0 + 64, k0);
+            tma_load_2d_pair(a_dst, &tma_a, bar, m0, k0, pol_a, ha);
+            tma_load_2d_pair(a_dst + 8192, &tma_a, bar, m0 + 64, k0, pol_a, ha);
           } else {
-            tma_load_2d_pair(a_dst, &tma_a, bar, k0, m0);
+            tma_load_2d_pair(a_dst, &tma_a, bar, k0, m0, pol_a, ha);
           }
           if (MODE == kDh || MODE == kDw) {
-            tma_load_2d_pair(b_dst, &tma_b, bar, n0, k0);
-            tma_load_2d_pair(b_dst + 8192, &tma_b, bar, n0 + 64, k0);
+            tma_load_2d_pair(b_dst, &tma_b, bar, n0, k0, pol_b, hb);
+            tma_load_2d_pair(b_dst + 8192, &tma_b, bar, n0 + 64, k0, pol_b, hb);
           } else {
-            tma_load_2d_pair(b_dst, &tma_b, bar, k0, n0);
+            tma_load_2d_pair(b_dst, &tma_b, bar, k0, n0, pol_b, hb);
           }
           ++issued;
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
