@@ -148,6 +148,23 @@ def _workload(args):
     return synth.workload(args.workload, **over)
 
 
+def reduce_over_ranks(elapsed, kept, world, device):
+    """(max elapsed over ranks, sum of kept rows over ranks).
+
+    Every rank scores its own batch (replicas, weak scaling), so the job's
+    time is the slowest rank's and its work is the sum of all ranks' rows.
+    """
+    if world <= 1:
+        return float(elapsed), float(kept)
+    import torch
+    import torch.distributed as dist
+    mx = torch.tensor([float(elapsed)], dtype=torch.float64, device=device)
+    sm = torch.tensor([float(kept)], dtype=torch.float64, device=device)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[0])
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -214,7 +231,7 @@ def run_ours(args):
 
     w = _workload(args)
     w = synth.workload(args.workload, N=w.N, V=w.V, seed=w.seed + 100 * rank)
-    inp = synth.make_inputs(w, device=dev)
+    inp = synth.make_inputs(w, device=dev, active_frac=args.active_frac)
     sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=args.chunk_rows, device=dev)
     comps = inp.get("components")
     lens = inp.get("seq_lens")
@@ -231,18 +248,25 @@ def run_ours(args):
     dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
     dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     ws = sc.workspace
-    g_ent = inp["grad_entropy"] if args.entropy_grad else None
+    use_ent_grad = (inp["grad_entropy"] is not None) if args.entropy_grad < 0 else bool(
+        args.entropy_grad)
+    g_ent = inp["grad_entropy"] if use_ent_grad else None
     stream = torch.cuda.current_stream(dev)
 
+    keep_arg = None if args.keep_off else keep  # keep-off arm: every row scored
+
     def step(hidden, targets, loss_mask, offs, g_lp, g_e):
-        if loss_mask is not None:
+        if args.keep_off:
+            pass
+        elif loss_mask is not None:
             L.lmhead_build_keep_mask(loss_mask, None, None, offs, keep, stream)
         else:
             keep.copy_(inp["keep"])
-        L.lmhead_fwd(hidden, inp["weight"], targets, keep, True, lp, ent, lse, ws,
+        L.lmhead_fwd(hidden, inp["weight"], targets, keep_arg, True, lp, ent, lse, ws,
                      args.chunk_rows, stream)
-        L.lmhead_bwd(hidden, inp["weight"], targets, keep, lse, ent, g_lp, g_e, dh, dW, False,
-                     ws, args.chunk_rows, stream)
+        if args.mode == "fwdbwd":
+            L.lmhead_bwd(hidden, inp["weight"], targets, keep_arg, lse, ent, g_lp, g_e, dh, dW,
+                         False, ws, args.chunk_rows, stream)
 
     loss_mask = comps[0] if comps is not None else None
     dev_args = (inp["hidden"], inp["targets"], loss_mask, offsets, inp["grad_logprob"], g_ent)
@@ -252,7 +276,7 @@ def run_ours(args):
     status = L.lmhead_get_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
-    nk = int(keep.sum().item())
+    nk = N if args.keep_off else int(keep.sum().item())
 
     # ---------------------------------------------------------- device-timed
     def barrier():
@@ -279,18 +303,11 @@ def run_ours(args):
         raise RuntimeError(f"device status {status_timed} after the timed steps")
     prof = L.lmhead_profile_read()
     ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms, float(nk)], device=dev, dtype=torch.float64)
-        mx = t.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        sm = t.clone()
-        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
-        ms_max, nk_total = float(mx[0]), float(sm[1])
-    else:
-        ms_max, nk_total = ms, float(nk)
+    ms_max, nk_total = reduce_over_ranks(ms, nk, world, dev)
     sec = ms_max / 1e3
     value = nk_total * args.steps / sec
-    flops_step = 8.0 * nk_total * H * V
+    per_row = 8.0 if args.mode == "fwdbwd" else 2.0
+    flops_step = per_row * nk_total * H * V
     tflops = flops_step * args.steps / sec / 1e12
     burst, sustained, hbm, peak_src = _peaks()
 
@@ -312,7 +329,7 @@ def run_ours(args):
                 "frac": None, "traffic": None}
     kernels = {k: {"launches": v[0], "ms": v[1], "share": v[1] / tot_ms} for k, v in kinds.items()}
     gemm_ms = sum(kinds[k][1] for k in gemm_flops if k in kinds)
-    gemm_tflops = 8.0 * nk * H * V * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms else None
+    gemm_tflops = per_row * nk * H * V * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms else None
 
     # ---------------------------------------------------------- end to end
     e2e = None
@@ -325,6 +342,10 @@ def run_ours(args):
         out_ent = torch.empty(N, dtype=torch.float32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
         d2h = 2 * N * 4
+        if args.keep_off:
+            host[2] = host[3] = None
+            dbuf[2] = dbuf[3] = None
+            h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
 
         def e2e_step():
             for d, hst in zip(dbuf, host):
@@ -343,10 +364,7 @@ def run_ours(args):
             e2e_step()
         barrier()
         el = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([el], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            el = float(t[0])
+        el, _ = reduce_over_ranks(el, 0, world, dev)
         if L.lmhead_get_status(ws) != 0:
             raise RuntimeError("device status non-zero after the end-to-end steps")
         e2e = {"value": nk_total * args.steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -371,9 +389,12 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": args.workload, "N": N, "H": H, "V": V, "kept_rows": nk,
                        "kept_frac": nk / N, "chunk_rows": args.chunk_rows or 8192,
-                       "entropy": "differentiable" if args.entropy_grad else "metric-only",
+                       "entropy": "differentiable" if g_ent is not None else "metric-only",
+                       "mode": args.mode, "keep_mask": "off" if args.keep_off else "on",
                        "l2": "inputs larger than L2 (W 1.2 GB, hidden 0.5 GB)",
                        "parallelism": f"replicas x{world}"},
+            "peak_device_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+            "logits_bf16_gb_avoided": N * V * 2 / 1e9,
             "tflops": tflops, "frac_of_peak": tflops / burst,
             "frac_of_sustained_peak": tflops / sustained,
             "gemm_tflops": gemm_tflops,
@@ -396,7 +417,13 @@ def main():
     ap.add_argument("--chunk-rows", type=int, default=0)
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling cases)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling cases)")
-    ap.add_argument("--entropy-grad", type=int, default=1)
+    ap.add_argument("--entropy-grad", type=int, default=-1,
+                    help="1: differentiable entropy, 0: metric-only (default: the workload's)")
+    ap.add_argument("--mode", default="fwdbwd", choices=["fwdbwd", "fwd"])
+    ap.add_argument("--keep-off", action="store_true",
+                    help="score every row (keep mask off), the comparison arm")
+    ap.add_argument("--active-frac", type=float, default=1.0,
+                    help="active suffix fraction of the entropy_bonus workload")
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
