@@ -28,8 +28,8 @@ enum GemmMode : int { kFwd = 0, kDz = 1, kDh = 2, kDw = 3 };
 
 struct TcGemmParams {
   const int32_t* d_nk;      // device Nk
-  int chunk_start;          // first compact row of this chunk
-  int chunk_rows;           // C: rows per chunk (multiple of 256)
+  int chunk_index;          // which chunk of the kept rows (see chunk_span)
+  int chunk_rows;           // C: most rows per chunk (multiple of 256)
   int V;
   int H;
   int group_n;              // N tiles per raster group (L2 reuse)
@@ -62,6 +62,29 @@ template <int MODE>
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                                 const TcGemmParams& p, int grid, cudaStream_t stream);
 
+// The Nk kept rows are cut into ceil(Nk / C) chunks of equal size rounded up
+// to 256 rows (so no chunk is much shorter than the others and the per-chunk
+// cost of the weight-gradient update stays hidden behind its MMAs).  Chunk c
+// covers compact rows [start, start + rows); rows == 0 past the last chunk.
+// Computed on the device from Nk, so the host never waits for Nk.
+__device__ __forceinline__ void chunk_span(int nk, int C, int c, int& start, int& rows) {
+  if (nk <= 0) {
+    start = 0;
+    rows = 0;
+    return;
+  }
+  const int nchunks = (nk + C - 1) / C;
+  if (c >= nchunks) {
+    start = nk;
+    rows = 0;
+    return;
+  }
+  const int per = (nk + nchunks - 1) / nchunks;
+  const int cb = (per + 255) & ~255;  // <= C because C is a multiple of 256
+  start = c * cb;
+  rows = nk - start < cb ? nk - start : cb;
+}
+
 // Rows counted by one block of the compaction scan (rowops.cu).
 constexpr int kCompactRowsPerBlock = 4096;
 
@@ -73,9 +96,9 @@ cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t 
                            int32_t* idx, int32_t* targets_c, int32_t* d_nk, int32_t* counts,
                            int* status, cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
-                               const int32_t* d_nk, int chunk_start, int chunk_rows, int H,
+                               const int32_t* d_nk, int chunk_index, int chunk_rows, int H,
                                __nv_bfloat16* hc, cudaStream_t s);
-cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_start,
+cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
                          float* lse_c, cudaStream_t s);
 cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,

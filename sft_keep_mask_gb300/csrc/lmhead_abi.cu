@@ -346,20 +346,21 @@ lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* 
   p.want_entropy = want_entropy ? 1 : 0;
   p.part = part;
 
-  for (int64_t cs = 0; cs < N; cs += L.C) {
+  const int64_t max_chunks = cdiv(N, L.C);
+  for (int64_t c = 0; c < max_chunks; ++c) {
     {
       Launch l(kKindGatherRows, s);
       LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
-                                static_cast<int>(cs), static_cast<int>(L.C), H, hc, s));
+                                static_cast<int>(c), static_cast<int>(L.C), H, hc, s));
     }
-    p.chunk_start = static_cast<int>(cs);
+    p.chunk_index = static_cast<int>(c);
     {
       Launch l(kKindGemmFwd, s);
       LM_TRY(run_gemm<kFwd>(pair, ma, mb, mb2, p, L.C, V, s));
     }
     {
       Launch l(kKindMerge, s);
-      LM_TRY(launch_merge(part, static_cast<int>(L.num_vt), d_nk, static_cast<int>(cs),
+      LM_TRY(launch_merge(part, static_cast<int>(L.num_vt), d_nk, static_cast<int>(c),
                           static_cast<int>(L.C), p.want_entropy, lp_c, ent_c, lse_c, s));
     }
   }
@@ -451,12 +452,13 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
   p.dw = dweight;
   const int64_t n_h_tiles = cdiv(H, kBN);
 
-  for (int64_t cs = 0; cs < N; cs += L.C) {
-    p.chunk_start = static_cast<int>(cs);
+  const int64_t max_chunks = cdiv(N, L.C);
+  for (int64_t c = 0; c < max_chunks; ++c) {
+    p.chunk_index = static_cast<int>(c);
     {
       Launch l(kKindGatherRows, s);
       LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
-                                static_cast<int>(cs), static_cast<int>(L.C), H, hc, s));
+                                static_cast<int>(c), static_cast<int>(L.C), H, hc, s));
     }
     {
       Launch l(kKindGemmDz, s);
@@ -471,7 +473,7 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
     {
       Launch l(kKindGemmDw, s);
       p.group_n = static_cast<int>(n_h_tiles);
-      p.beta = (cs > 0 || dw_accumulate) ? 1 : 0;
+      p.beta = (c > 0 || dw_accumulate) ? 1 : 0;
       LM_TRY(run_gemm<kDw>(pair, m_dz_mn, m_hc_mn, m_hc_mn, p, V, H, s));
     }
   }

@@ -134,11 +134,10 @@ __global__ void scatter_kernel(const uint8_t* __restrict__ keep,
 // contraction as zero K rows).  One warp per row, 16-byte vectors.
 __global__ void gather_rows_kernel(const uint4* __restrict__ hidden,
                                    const int32_t* __restrict__ idx, const int32_t* d_nk,
-                                   int chunk_start, int chunk_rows, int vec_per_row,
+                                   int chunk_index, int chunk_rows, int vec_per_row,
                                    uint4* __restrict__ hc) {
-  const int nk = *d_nk;
-  int rows = nk - chunk_start;
-  rows = rows < 0 ? 0 : (rows > chunk_rows ? chunk_rows : rows);
+  int chunk_start, rows;
+  chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   const int padded = (rows + 255) & ~255;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int l = threadIdx.x & 31;
@@ -169,12 +168,11 @@ __global__ void gather_vec_kernel(const int32_t* __restrict__ idx, const int32_t
 //   M = max m_i, S = sum s_i e^(m_i - M), U = sum e^(m_i - M)(u_i + s_i (m_i - M))
 //   lse = M + log S, logprob = t - lse, entropy = log S - U / S.
 __global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const int32_t* d_nk,
-                             int chunk_start, int chunk_rows, int want_entropy,
+                             int chunk_index, int chunk_rows, int want_entropy,
                              float* __restrict__ lp_c, float* __restrict__ ent_c,
                              float* __restrict__ lse_c) {
-  const int nk = *d_nk;
-  int rows = nk - chunk_start;
-  rows = rows < 0 ? 0 : (rows > chunk_rows ? chunk_rows : rows);
+  int chunk_start, rows;
+  chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= rows) return;
   float M = -INFINITY;
@@ -257,19 +255,19 @@ cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t 
 }
 
 cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
-                               const int32_t* d_nk, int chunk_start, int chunk_rows, int H,
+                               const int32_t* d_nk, int chunk_index, int chunk_rows, int H,
                                __nv_bfloat16* hc, cudaStream_t s) {
   const int vec = H / 8;
   gather_rows_kernel<<<blocks_for(chunk_rows, 8), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(hidden), idx, d_nk, chunk_start, chunk_rows, vec,
+      reinterpret_cast<const uint4*>(hidden), idx, d_nk, chunk_index, chunk_rows, vec,
       reinterpret_cast<uint4*>(hc));
   return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_start,
+cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
                          float* lse_c, cudaStream_t s) {
-  merge_kernel<<<blocks_for(chunk_rows, 128), 128, 0, s>>>(part, num_vt, d_nk, chunk_start,
+  merge_kernel<<<blocks_for(chunk_rows, 128), 128, 0, s>>>(part, num_vt, d_nk, chunk_index,
                                                            chunk_rows, want_entropy, lp_c, ent_c,
                                                            lse_c);
   return cudaGetLastError();

@@ -58,19 +58,20 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 //   tbase      TMEM address of (this warp's lane quarter, column 0 of the tile)
 //   row        kFwd/kDz/kDh: row within the chunk; kDw: vocabulary row
 //   nt         column tile
+//   cstart     first compact row of the chunk
 //   rows_valid rows of the chunk that hold kept tokens
 //   have_acc   false only for kDw with an empty K range (writes zeros)
 //   release    called once, right after the last TMEM load of the tile
 template <int MODE, typename Release>
 __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tbase, int row,
-                                              int nt, int rows_valid, bool have_acc,
+                                              int nt, int cstart, int rows_valid, bool have_acc,
                                               Release&& release) {
   constexpr int kSlices = kBN / 32;
   const int col_tile = nt * kBN;
 
   if (MODE == kFwd) {
     const bool row_ok = row < rows_valid;
-    const int y = row_ok ? p.targets_c[p.chunk_start + row] : -1;
+    const int y = row_ok ? p.targets_c[cstart + row] : -1;
     const bool tail = col_tile + kBN > p.V;
     float m2 = -INFINITY, s = 0.f, u2 = 0.f, tz = -INFINITY;
 #pragma unroll 1
@@ -140,7 +141,7 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
     float lse2 = 0.f, ca = 0.f, cb = 0.f, glp = 0.f;
     int y = -1;
     if (row_ok) {
-      const int cr = p.chunk_start + row;
+      const int cr = cstart + row;
       lse2 = p.lse_c[cr] * kLog2e;
       glp = p.glp_c[cr];
       y = p.targets_c[cr];
@@ -191,7 +192,7 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
     }
   } else if (MODE == kDh) {
     const bool row_ok = row < rows_valid;
-    const int64_t orow = row_ok ? p.idx[p.chunk_start + row] : 0;
+    const int64_t orow = row_ok ? p.idx[cstart + row] : 0;
     __nv_bfloat16* hrow = p.dhidden + orow * p.H;
 #pragma unroll 1
     for (int c = 0; c < kSlices; ++c) {
@@ -251,15 +252,13 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
 // Problem extents of a contraction for this chunk (the number of kept rows
 // lives on the device).  Returns false when the launch has nothing to do.
 template <int MODE>
-__device__ __forceinline__ bool gemm_extents(const TcGemmParams& p, int& rows_valid, int& M,
-                                             int& N, int& K) {
-  const int nk = *p.d_nk;
-  rows_valid = nk - p.chunk_start;
-  rows_valid = rows_valid < 0 ? 0 : (rows_valid > p.chunk_rows ? p.chunk_rows : rows_valid);
+__device__ __forceinline__ bool gemm_extents(const TcGemmParams& p, int& cstart, int& rows_valid,
+                                             int& M, int& N, int& K) {
+  chunk_span(*p.d_nk, p.chunk_rows, p.chunk_index, cstart, rows_valid);
   if (MODE == kDw) {
     M = p.V; N = p.H; K = rows_valid;
     // An empty first chunk still has to clear dW when it is not accumulated.
-    return !(rows_valid == 0 && (p.beta || p.chunk_start > 0));
+    return !(rows_valid == 0 && (p.beta || p.chunk_index > 0));
   }
   if (MODE == kDh) {
     M = rows_valid; N = p.H; K = p.V;

@@ -54,8 +54,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  int rows_valid, M, N, K;
-  if (!gemm_extents<MODE>(p, rows_valid, M, N, K)) return;
+  int cstart, rows_valid, M, N, K;
+  if (!gemm_extents<MODE>(p, cstart, rows_valid, M, N, K)) return;
   const int num_m = (M + kBM - 1) / kBM;
   const int num_n = (N + kBN - 1) / kBN;
   const int num_kb = (K + kBK - 1) / kBK;
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
       uint64_t* te = &tempty[acc];
-      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, rows_valid, num_kb > 0, [&] {
+      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, cstart, rows_valid, num_kb > 0, [&] {
         tc_fence_before();
         mbar_arrive(te);
       });

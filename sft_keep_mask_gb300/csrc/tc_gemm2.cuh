@@ -53,8 +53,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
-  int rows_valid, M, N, K;
-  if (!gemm_extents<MODE>(p, rows_valid, M, N, K)) return;  // uniform over the grid
+  int cstart, rows_valid, M, N, K;
+  if (!gemm_extents<MODE>(p, cstart, rows_valid, M, N, K)) return;  // uniform over the grid
   const int num_m = (M + kPairTileM - 1) / kPairTileM;
   const int num_n = (N + kBN - 1) / kBN;
   const int num_kb = (K + kBK - 1) / kBK;
@@ -194,7 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
       const uint32_t te = map_to_cta(smem_addr(&tempty[acc]), 0);
-      epilogue_tile<MODE>(p, tbase, mt * kPairTileM + row_local, nt, rows_valid, num_kb > 0,
+      epilogue_tile<MODE>(p, tbase, mt * kPairTileM + row_local, nt, cstart, rows_valid, num_kb > 0,
                           [&] {
                             tc_fence_before();
                             __syncwarp();

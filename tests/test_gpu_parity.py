@@ -307,3 +307,13 @@ def test_variants_agree_bitwise():
             del os.environ["LMHEAD_GEMM"]
     for a, b in zip(*res):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("nk", [255, 256, 257, 511, 513, 1000])
+def test_chunk_boundaries(nk):
+    # the kept rows are cut into equal 256-aligned chunks on the device; Nk
+    # around chunk multiples exercises the first / last chunk bounds
+    w = synth.workload("tiny", seed=30 + nk, N=1100, H=64, V=300)
+    keep = np.zeros(w.N, np.uint8)
+    keep[np.random.default_rng(nk).choice(w.N, nk, replace=False)] = 1
+    _run_both(w, keep_override=keep, chunk_rows=256)
