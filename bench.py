@@ -407,6 +407,71 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_sls(args):
+    """Scoring of existing bf16 logits (selective_log_softmax), fwd + bwd."""
+    import torch
+    from sft_keep_mask_gb300 import lmhead as L
+    from sft_keep_mask_gb300 import synth
+    world, rank, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L.lib()
+    N, V = (args.rows or 16384), (args.vocab or 151936)
+    d = synth.make_logits(N, V, seed=60 + rank, device=dev)
+    z = d["logits"]
+    lp = torch.empty(N, device=dev)
+    ent = torch.empty(N, device=dev)
+    lse = torch.empty(N, device=dev)
+    dz = torch.empty_like(z)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        L.lmhead_selective_log_softmax_fwd(z, d["targets"], None, True, lp, ent, lse, st, stream)
+        L.lmhead_selective_log_softmax_bwd(z, d["targets"], None, lse, ent, d["grad_logprob"],
+                                           d["grad_entropy"], dz, st, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    L.lmhead_profile_enable(True)
+    L.lmhead_profile_read()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    L.lmhead_profile_enable(False)
+    prof = L.lmhead_profile_read()
+    if int(st.item()) != 0:
+        raise RuntimeError("device status non-zero")
+    ms = e0.elapsed_time(e1)
+    _, _, hbm, src = _peaks()
+    elem = float(N) * V
+    fwd_ms, bwd_ms = prof["sls_fwd"][1], prof["sls_bwd"][1]
+    fwd_gbs = 2 * elem * args.steps / (fwd_ms / 1e3) / 1e9
+    bwd_gbs = 4 * elem * args.steps / (bwd_ms / 1e3) / 1e9
+    dom, ach = ("sls_bwd", bwd_gbs) if bwd_ms >= fwd_ms else ("sls_fwd", fwd_gbs)
+    line = {
+        "metric": "selective_log_softmax fwd+bwd rows/s (HBM GB/s of measured peak)",
+        "value": N * args.steps / (ms / 1e3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "selective_log_softmax", "N": N, "V": V,
+                   "logits": "bf16 ~N(0, 4)", "l2": "inputs larger than L2 (5 GB logits)"},
+        "gbs": {"sls_fwd": fwd_gbs, "sls_bwd": bwd_gbs},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                     "frac": ach / hbm, "peak_source": src, "traffic": None},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,6 +495,8 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "selective_log_softmax":
+        run_sls(args)
     else:
         run_ours(args)
 

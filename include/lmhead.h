@@ -199,6 +199,51 @@ lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64_t* targets
 lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t* d_nk,
                             int64_t N, float* dst, lmhead_stream_t stream);
 
+/* Element types of a logit matrix. */
+#define LMHEAD_DTYPE_BF16 0
+#define LMHEAD_DTYPE_F32 1
+
+/*
+ * Scoring of logits that already exist ([P3] section 1, the chunked float32
+ * `selective_log_softmax`): for every kept row i of a logit matrix z[N, V],
+ *   lse[i] = log sum_v exp(z_iv), logprob[i] = z_{i,y_i} - lse[i],
+ *   entropy[i] = -sum_v p_iv log p_iv, computed and returned in float32 (no
+ *   bf16 quantisation of the log-prob).  Bound by HBM bandwidth (one read of
+ *   the logits).
+ *   logits : [N, V] row-major with row stride ld elements (ld >= V), element
+ *            type logits_dtype (LMHEAD_DTYPE_BF16 or LMHEAD_DTYPE_F32).  16-byte
+ *            aligned rows take the vectorised path; others are still correct.
+ *   targets, keep : as for lmhead_fwd (keep nullable = all rows kept).
+ *   logprob, lse (out) : float32 [N]; entropy (out) float32 [N], may be NULL
+ *            iff want_entropy == 0.  Skipped rows get +0.0.
+ *   d_status (out, nullable) : int32 [1] on the device, set to LMHEAD_ETARGET
+ *            if a kept row's target is outside [0, V) (the caller clears it);
+ *            such a row is scored against target 0.
+ */
+lmhead_status lmhead_selective_log_softmax_fwd(const void* logits, int logits_dtype, int64_t ld,
+                                               const int64_t* targets, const uint8_t* keep,
+                                               int64_t N, int V, int want_entropy,
+                                               float* logprob, float* entropy, float* lse,
+                                               int32_t* d_status, lmhead_stream_t stream);
+
+/*
+ * Backward of the above: dlogits[i, v] = g_lp (1[v = y] - p) - g_ent p (log p + H)
+ * with p recomputed from the logits and the forward's lse and entropy
+ * ([P3] section 1: the softmax is recomputed, not saved).
+ *   lse, entropy : float32 [N] from the forward (entropy read only when
+ *            grad_entropy is given).
+ *   grad_logprob : float32 [N]; grad_entropy : float32 [N], nullable.
+ *   dlogits (out) : [N, V] of the logits' element type, row stride ld_out;
+ *            rows of skipped tokens are written as 0.  May not alias logits.
+ */
+lmhead_status lmhead_selective_log_softmax_bwd(const void* logits, int logits_dtype, int64_t ld,
+                                               const int64_t* targets, const uint8_t* keep,
+                                               int64_t N, int V, const float* lse,
+                                               const float* entropy, const float* grad_logprob,
+                                               const float* grad_entropy, void* dlogits,
+                                               int64_t ld_out, int32_t* d_status,
+                                               lmhead_stream_t stream);
+
 /*
  * Device-side status of the last lmhead_* call that used this workspace:
  * synchronises `stream`, then returns LMHEAD_OK, LMHEAD_ETARGET or

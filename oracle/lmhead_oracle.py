@@ -45,6 +45,10 @@ notes of the repository):
 * With ``g_ent is None`` (metric-only entropy) the entropy term is absent from
   the logit gradient.
 
+Also the scoring of logits that already exist ([P3] section 1,
+``selective_log_softmax``): the same log-prob / entropy / lse definitions and
+their logit gradient, applied to a given ``[N, V]`` logit matrix.
+
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (closed forms, invariants, brute force on tiny inputs, central finite
 differences).  No function is "parity unpinned".
@@ -219,3 +223,57 @@ def score_rows(h_rows, W, targets_rows, g_lp_rows=None, g_ent_rows=None,
         return lp, ent, lse, None, None
     dh, dW = backward(h_rows, W, targets_rows, keep, g_lp_rows, g_ent_rows)
     return lp, ent, lse, dh, dW
+
+
+def selective_log_softmax(z, targets, keep=None, want_entropy=True):
+    """Log-prob of the target, entropy and lse of rows of given logits.
+
+    [P3] section 1 ("selective_log_softmax pins one full-vocab copy per row"):
+    log_softmax of each row computed in float (here float64), the target's
+    log-prob gathered, and the entropy -(p * log p) summed over the
+    vocabulary ([P2] gemini-code-assist review).  Rows with keep == 0 get 0.
+
+    z [N, V] (any float dtype; upcast to float64), targets [N] int,
+    keep [N] 0/1 or None.  Returns (logprob, entropy, lse), float64 [N].
+    """
+    z = np.asarray(z, dtype=np.float64)
+    n, V = z.shape
+    idx, nk, yc = compact(keep, targets, V)
+    lp = np.zeros(n)
+    ent = np.zeros(n)
+    lse = np.zeros(n)
+    if nk == 0:
+        return lp, ent, lse
+    logp, l = _log_softmax(z[idx])
+    lp[idx] = logp[np.arange(nk), yc]
+    lse[idx] = l
+    if want_entropy:
+        ent[idx] = -(np.exp(logp) * logp).sum(axis=1)
+    return lp, ent, lse
+
+
+def selective_log_softmax_backward(z, targets, keep, g_lp, g_ent=None):
+    """Gradient of sum_i g_lp[i] logprob[i] + g_ent[i] entropy[i] w.r.t. z.
+
+    The same logit gradient as ``backward``:
+    dz_v = g_lp (1[v=y] - p_v) - g_ent p_v (log p_v + entropy); rows with
+    keep == 0 get 0.  Returns dz, float64 [N, V].
+    """
+    z = np.asarray(z, dtype=np.float64)
+    n, V = z.shape
+    idx, nk, yc = compact(keep, targets, V)
+    dz = np.zeros((n, V))
+    if nk == 0:
+        return dz
+    logp, _ = _log_softmax(z[idx])
+    p = np.exp(logp)
+    onehot = np.zeros_like(p)
+    onehot[np.arange(nk), yc] = 1.0
+    g1 = np.asarray(g_lp, dtype=np.float64)[idx]
+    d = g1[:, None] * (onehot - p)
+    if g_ent is not None:
+        g2 = np.asarray(g_ent, dtype=np.float64)[idx]
+        ent = -(p * logp).sum(axis=1)
+        d = d - g2[:, None] * p * (logp + ent[:, None])
+    dz[idx] = d
+    return dz

@@ -18,6 +18,8 @@ from .lmhead import (  # noqa: F401
     lmhead_launch_count,
     lmhead_profile_enable,
     lmhead_profile_read,
+    lmhead_selective_log_softmax_bwd,
+    lmhead_selective_log_softmax_fwd,
     lmhead_strerror,
     lmhead_version,
     lmhead_workspace_size,

@@ -112,6 +112,15 @@ cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N
 cudaError_t launch_zero_skipped_rows(const uint8_t* keep, int64_t N, int H,
                                      __nv_bfloat16* dhidden, cudaStream_t s);
 
+// Scoring of existing logits (logits_sls.cu); dtype 0 = bf16, 1 = float32.
+cudaError_t launch_sls_fwd(const void* logits, int dtype, int64_t ld, const int64_t* targets,
+                           const uint8_t* keep, int64_t N, int V, int want_entropy, float* lp,
+                           float* ent, float* lse, int* status, cudaStream_t s);
+cudaError_t launch_sls_bwd(const void* logits, int dtype, int64_t ld, const int64_t* targets,
+                           const uint8_t* keep, int64_t N, int V, const float* lse,
+                           const float* ent, const float* g_lp, const float* g_ent, void* dz,
+                           int64_t ld_out, int* status, cudaStream_t s);
+
 int device_sm_count();
 
 }  // namespace lmhead

@@ -69,11 +69,13 @@ T* at(void* ws, size_t off) {
 // ------------------------------------------------------------ profiling
 enum Kind : int {
   kKindBuildKeep = 0, kKindCompact, kKindGatherRows, kKindGemmFwd, kKindMerge, kKindExpand,
-  kKindGatherVec, kKindZeroRows, kKindGemmDz, kKindGemmDh, kKindGemmDw, kNumKinds
+  kKindGatherVec, kKindZeroRows, kKindGemmDz, kKindGemmDh, kKindGemmDw, kKindSlsFwd,
+  kKindSlsBwd, kNumKinds
 };
 const char* kKindNames[kNumKinds] = {"build_keep", "compact",  "gather_rows", "gemm_fwd",
                                      "merge",      "expand",   "gather_vec",  "zero_rows",
-                                     "gemm_dz",    "gemm_dh",  "gemm_dw"};
+                                     "gemm_dz",    "gemm_dh",  "gemm_dw",     "sls_fwd",
+                                     "sls_bwd"};
 
 std::atomic<int64_t> g_launches{0};
 std::mutex g_prof_mu;
@@ -489,6 +491,46 @@ lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Launch l(kKindExpand, s);
   return cuda_status(launch_expand(src, idx, d_nk, N, dst, s));
+}
+
+lmhead_status lmhead_selective_log_softmax_fwd(const void* logits, int logits_dtype, int64_t ld,
+                                               const int64_t* targets, const uint8_t* keep,
+                                               int64_t N, int V, int want_entropy,
+                                               float* logprob, float* entropy, float* lse,
+                                               int32_t* d_status, lmhead_stream_t stream) {
+  if (N < 0 || N > 2147483647LL || V < 1 || ld < V || (logits_dtype != 0 && logits_dtype != 1))
+    return LMHEAD_EINVAL;
+  if (logits == nullptr || targets == nullptr || logprob == nullptr || lse == nullptr ||
+      (want_entropy && entropy == nullptr))
+    return LMHEAD_EINVAL;
+  if (N == 0) return LMHEAD_OK;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch l(kKindSlsFwd, s);
+  return cuda_status(launch_sls_fwd(logits, logits_dtype, ld, targets, keep, N, V,
+                                    want_entropy ? 1 : 0, logprob, want_entropy ? entropy : nullptr,
+                                    lse, d_status, s));
+}
+
+lmhead_status lmhead_selective_log_softmax_bwd(const void* logits, int logits_dtype, int64_t ld,
+                                               const int64_t* targets, const uint8_t* keep,
+                                               int64_t N, int V, const float* lse,
+                                               const float* entropy, const float* grad_logprob,
+                                               const float* grad_entropy, void* dlogits,
+                                               int64_t ld_out, int32_t* d_status,
+                                               lmhead_stream_t stream) {
+  if (N < 0 || N > 2147483647LL || V < 1 || ld < V || ld_out < V ||
+      (logits_dtype != 0 && logits_dtype != 1))
+    return LMHEAD_EINVAL;
+  if (logits == nullptr || targets == nullptr || lse == nullptr || grad_logprob == nullptr ||
+      dlogits == nullptr || (grad_entropy != nullptr && entropy == nullptr) || dlogits == logits)
+    return LMHEAD_EINVAL;
+  if (N == 0) return LMHEAD_OK;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch l(kKindSlsBwd, s);
+  return cuda_status(launch_sls_bwd(logits, logits_dtype, ld, targets, keep, N, V, lse, entropy,
+                                    grad_logprob, grad_entropy, dlogits, ld_out, d_status, s));
 }
 
 lmhead_status lmhead_get_status(const void* workspace, lmhead_stream_t stream) {

@@ -45,6 +45,10 @@ _SIGS = {
     "lmhead_bwd": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                           _I32, _I32, _VP, ctypes.c_size_t, _VP]),
     "lmhead_expand": (_I32, [_VP, _VP, _VP, _I64, _VP, _VP]),
+    "lmhead_selective_log_softmax_fwd": (_I32, [_VP, _I32, _I64, _VP, _VP, _I64, _I32, _I32, _VP,
+                                                _VP, _VP, _VP, _VP]),
+    "lmhead_selective_log_softmax_bwd": (_I32, [_VP, _I32, _I64, _VP, _VP, _I64, _I32, _VP, _VP,
+                                                _VP, _VP, _VP, _I64, _VP, _VP]),
     "lmhead_get_status": (_I32, [_VP, _VP]),
     "lmhead_strerror": (ctypes.c_char_p, [_I32]),
     "lmhead_profile_enable": (None, [_I32]),
@@ -185,6 +189,56 @@ def lmhead_expand(src, idx, d_nk, N, dst, stream=None):
     _need(dst, torch.float32, "dst", N)
     code = lib().lmhead_expand(_p(src), _p(idx), _p(d_nk), N, _p(dst), _s(stream))
     _check(code, "lmhead_expand")
+
+
+def _logits_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return 0
+    if t.dtype == torch.float32:
+        return 1
+    raise TypeError("logits must be bf16 or float32")
+
+
+def _rows(t, name):
+    if not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+        raise TypeError(f"{name} must be a 2-D CUDA tensor with unit column stride")
+    return t.stride(0)
+
+
+def lmhead_selective_log_softmax_fwd(logits, targets, keep, want_entropy, logprob, entropy, lse,
+                                     d_status=None, stream=None):
+    N, V = logits.shape
+    ld = _rows(logits, "logits")
+    _need(targets, torch.int64, "targets", N)
+    _need(keep, torch.uint8, "keep", N)
+    _need(logprob, torch.float32, "logprob", N)
+    _need(entropy, torch.float32, "entropy", N)
+    _need(lse, torch.float32, "lse", N)
+    _need(d_status, torch.int32, "d_status", 1)
+    code = lib().lmhead_selective_log_softmax_fwd(
+        _p(logits), _logits_dtype(logits), ld, _p(targets), _p(keep), N, V,
+        int(bool(want_entropy)), _p(logprob), _p(entropy), _p(lse), _p(d_status), _s(stream))
+    _check(code, "lmhead_selective_log_softmax_fwd")
+
+
+def lmhead_selective_log_softmax_bwd(logits, targets, keep, lse, entropy, grad_logprob,
+                                     grad_entropy, dlogits, d_status=None, stream=None):
+    N, V = logits.shape
+    ld = _rows(logits, "logits")
+    ld_out = _rows(dlogits, "dlogits")
+    if dlogits.dtype != logits.dtype or tuple(dlogits.shape) != (N, V):
+        raise TypeError("dlogits must match the logits' shape and dtype")
+    _need(targets, torch.int64, "targets", N)
+    _need(keep, torch.uint8, "keep", N)
+    _need(lse, torch.float32, "lse", N)
+    _need(entropy, torch.float32, "entropy", N)
+    _need(grad_logprob, torch.float32, "grad_logprob", N)
+    _need(grad_entropy, torch.float32, "grad_entropy", N)
+    _need(d_status, torch.int32, "d_status", 1)
+    code = lib().lmhead_selective_log_softmax_bwd(
+        _p(logits), _logits_dtype(logits), ld, _p(targets), _p(keep), N, V, _p(lse), _p(entropy),
+        _p(grad_logprob), _p(grad_entropy), _p(dlogits), ld_out, _p(d_status), _s(stream))
+    _check(code, "lmhead_selective_log_softmax_bwd")
 
 
 def lmhead_get_status(workspace, stream=None) -> int:

@@ -156,3 +156,24 @@ def sample_rows(n_kept: int, count: int, seed: int):
     rng = np.random.default_rng(1000 + seed)
     count = min(count, n_kept)
     return np.sort(rng.choice(n_kept, size=count, replace=False))
+
+
+def make_logits(N: int, V: int, seed: int, std: float = 2.0, dtype=torch.bfloat16,
+                device="cpu", ld: int = 0):
+    """Logits ~ N(0, std^2) of shape [N, V] (row stride ld >= V when given),
+    targets ~ U[0, V), grad_logprob ~ N(0, 1) and grad_entropy ~ N(0, 0.1).
+    The shape of twinkle pull request #283's measurements is N=16384,
+    V=151936."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    width = max(ld, V)
+    z = torch.empty(N, width, dtype=dtype, device=dev)
+    rows = 2048
+    for r in range(0, N, rows):
+        blk = torch.randn(min(rows, N - r), width, generator=g, device=dev)
+        z[r:r + blk.shape[0]] = (blk * std).to(dtype)
+    targets = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int64)
+    g_lp = torch.randn(N, generator=g, device=dev)
+    g_ent = 0.1 * torch.randn(N, generator=g, device=dev)
+    return dict(logits=z[:, :V], targets=targets, grad_logprob=g_lp, grad_entropy=g_ent)

@@ -363,3 +363,85 @@ def test_score_rows_matches_full_batch():
     np.testing.assert_allclose(r[1], ent[rows], atol=1e-13)
     np.testing.assert_allclose(r[2], lse[rows], atol=1e-13)
     np.testing.assert_allclose(r[3], dh[rows], atol=1e-13)
+
+
+# ------------------------------------------- scoring of existing logits
+
+def test_sls_brute_force_and_zero_fill():
+    rng = np.random.default_rng(40)
+    z = 3.0 * rng.standard_normal((7, 11))
+    y = rng.integers(0, 11, 7)
+    keep = np.array([1, 0, 1, 1, 0, 1, 1], np.uint8)
+    lp, ent, lse = O.selective_log_softmax(z, y, keep)
+    for i in range(7):
+        if not keep[i]:
+            assert lp[i] == 0 and ent[i] == 0 and lse[i] == 0
+            continue
+        row = list(z[i])
+        m = max(row)
+        l = m + math.log(sum(math.exp(v - m) for v in row))
+        e = -sum(math.exp(v - l) * (v - l) for v in row)
+        assert abs(lp[i] - (row[y[i]] - l)) < 1e-12
+        assert abs(ent[i] - e) < 1e-12 and abs(lse[i] - l) < 1e-12
+
+
+def test_sls_closed_forms():
+    g = _read_golden("closed_forms.txt")
+    V = 4096
+    lp, ent, lse = O.selective_log_softmax(np.full((2, V), 1.5), np.array([3, 9]))
+    np.testing.assert_allclose(ent, g[("uniform_4096", "entropy")], atol=1e-12)
+    np.testing.assert_allclose(lp, -g[("uniform_4096", "entropy")], atol=1e-12)
+    np.testing.assert_allclose(lse, 1.5 + g[("uniform_4096", "entropy")], atol=1e-12)
+    lp, ent, lse = O.selective_log_softmax(np.array([[0.0, math.log(3.0)]]), np.array([0]))
+    assert abs(lp[0] - g[("two_way", "logprob")]) < 1e-14
+    assert abs(ent[0] - g[("two_way", "entropy")]) < 1e-14
+
+
+def test_sls_row_shift_invariance():
+    rng = np.random.default_rng(41)
+    z = rng.standard_normal((20, 50))
+    y = rng.integers(0, 50, 20)
+    c = 100 * rng.standard_normal(20)
+    a = O.selective_log_softmax(z, y)
+    b = O.selective_log_softmax(z + c[:, None], y)
+    np.testing.assert_allclose(b[0], a[0], atol=1e-10)
+    np.testing.assert_allclose(b[1], a[1], atol=1e-10)
+    np.testing.assert_allclose(b[2], a[2] + c, atol=1e-10)
+
+
+def test_sls_agrees_with_the_fused_forward_and_backward():
+    h, W, y, keep, g_lp, g_ent = _problem(42, 30, 12, 40)
+    z = h @ W.T
+    for a, b in zip(O.selective_log_softmax(z, y, keep), O.forward(h, W, y, keep)):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+    dz = O.selective_log_softmax_backward(z, y, keep, g_lp, g_ent)
+    dh, dW = O.backward(h, W, y, keep, g_lp, g_ent)
+    np.testing.assert_allclose(dz @ W, dh, atol=1e-11)
+    np.testing.assert_allclose(dz.T @ h, dW, atol=1e-11)
+
+
+@pytest.mark.parametrize("with_entropy", [True, False])
+def test_sls_backward_finite_differences(with_entropy):
+    rng = np.random.default_rng(43)
+    z = 2.0 * rng.standard_normal((3, 9))
+    y = rng.integers(0, 9, 3)
+    keep = np.array([1, 1, 0], np.uint8)
+    g1 = rng.standard_normal(3)
+    g2 = 0.5 * rng.standard_normal(3) if with_entropy else None
+
+    def loss(zz):
+        lp, ent, _ = O.selective_log_softmax(zz, y, keep)
+        return float(np.sum(g1 * lp) + (np.sum(g2 * ent) if g2 is not None else 0.0))
+
+    dz = O.selective_log_softmax_backward(z, y, keep, g1, g2)
+    num = np.zeros_like(z)
+    eps = 1e-5
+    for i in range(3):
+        for v in range(9):
+            zp, zm = z.copy(), z.copy()
+            zp[i, v] += eps
+            zm[i, v] -= eps
+            num[i, v] = (loss(zp) - loss(zm)) / (2 * eps)
+    assert np.linalg.norm(dz - num) <= 1e-7 * max(np.linalg.norm(num), 1.0)
+    np.testing.assert_allclose(dz.sum(axis=1), 0.0, atol=1e-12)
+    assert not dz[2].any()
