@@ -42,6 +42,36 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def kernel_source_digest():
+    """sha256 over the library's CUDA sources (csrc/), in name order."""
+    import hashlib
+    d = os.path.join(ROOT, "sft_keep_mask_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, config):
+    """DRAM bytes per launch of `kernel` from an ncu capture of this workload,
+    or None if no capture of the current kernel sources exists."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_sha256") != kernel_source_digest():
+        return None
+    for key in ("workload", "N", "H", "V", "chunk_rows", "mode", "keep_mask"):
+        if rec.get("config", {}).get(key) != config.get(key):
+            return None
+    return rec.get("kernels", {}).get(kernel)
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -402,6 +432,13 @@ def run_ours(args):
             "clocks": clk.summary(), "device_status": status_timed, "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        rec = recorded_traffic(roof["kernel"], line["config"])
+        if rec is not None:
+            roof["traffic"] = rec["dram_bytes_per_launch"]
+            roof["traffic_note"] = (
+                "ncu dram__bytes_read.sum + dram__bytes_write.sum of this kernel over one step "
+                "of this workload / its launches per step (capture of the current sources); "
+                f"algorithmic bytes per launch {rec['algorithmic_bytes_per_launch']:.4g}")
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -190,6 +190,43 @@ lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64_t* targets
                                      int32_t* d_status, lmhead_stream_t stream);
 
 /*
+ * Vocabulary-parallel form ([P2] gemini-code-assist review: with the LM head
+ * split over the vocabulary, each rank reduces its own logits and one
+ * exchange after the loop completes the log-softmax and the entropy; greptile
+ * / cursor reviews: the fused op returns the rank-local dZ W hidden gradient
+ * and the caller reduces it).  A rank holds W[v_begin : v_begin + V_shard].
+ *
+ * lmhead_fwd_shard: per kept row, the shard's partial reduction
+ *     partials[i] = (m, s, u, t) with m = max_v z_v, s = sum exp(z_v - m),
+ *     u = sum exp(z_v - m)(z_v - m), t = z_y if y is in the shard else -inf;
+ *     float32 [N, 4], 16-byte aligned; skipped rows get (-inf, 0, 0, -inf).
+ *   targets are global vocabulary ids, checked against [0, V_total).
+ *   Other arguments as for lmhead_fwd (V = V_shard).
+ * lmhead_merge_shards: partials of all shards, float32 [num_shards, N, 4]
+ *   (e.g. gathered across ranks by the caller), -> logprob, entropy, lse
+ *   [N] (skipped rows +0.0).
+ * lmhead_bwd_shard: as lmhead_bwd for the shard, with the merged (whole
+ *   vocabulary) lse and entropy; dhidden_partial (bf16 [N, H]) receives this
+ *   shard's dZ W_shard, to be summed over shards by the caller; dweight_shard
+ *   is float32 [V_shard, H].
+ */
+lmhead_status lmhead_fwd_shard(const void* hidden, const void* weight_shard,
+                               const int64_t* targets, const uint8_t* keep, int64_t N, int H,
+                               int V_shard, int64_t v_begin, int64_t V_total, int want_entropy,
+                               float* partials, int chunk_rows, void* workspace,
+                               size_t ws_bytes, lmhead_stream_t stream);
+lmhead_status lmhead_merge_shards(const float* partials, int num_shards, const uint8_t* keep,
+                                  int64_t N, int want_entropy, float* logprob, float* entropy,
+                                  float* lse, lmhead_stream_t stream);
+lmhead_status lmhead_bwd_shard(const void* hidden, const void* weight_shard,
+                               const int64_t* targets, const uint8_t* keep, int64_t N, int H,
+                               int V_shard, int64_t v_begin, int64_t V_total, const float* lse,
+                               const float* entropy, const float* grad_logprob,
+                               const float* grad_entropy, void* dhidden_partial,
+                               float* dweight_shard, int dw_accumulate, int chunk_rows,
+                               void* workspace, size_t ws_bytes, lmhead_stream_t stream);
+
+/*
  * Expand compacted per-row values back to all rows ([P1] Overview: expand
  * back, skipped positions get zeros).
  *   src  : float32 [Nk]   idx : int32 [Nk] (from lmhead_compact)

@@ -277,3 +277,69 @@ def selective_log_softmax_backward(z, targets, keep, g_lp, g_ent=None):
         d = d - g2[:, None] * p * (logp + ent[:, None])
     dz[idx] = d
     return dz
+
+
+def shard_partials(h, W_shard, v_begin, targets, keep=None):
+    """Per-row partial reductions over one vocabulary shard.
+
+    [P2] gemini-code-assist review: with the LM head split over the vocabulary
+    (tensor parallel), each rank reduces its own logits and a single exchange
+    after the chunk loop completes the log-softmax and the entropy.  For the
+    shard W_shard = W[v_begin : v_begin + Vs] and each kept row:
+      m = max_v z_v,  s = sum_v exp(z_v - m),
+      u = sum_v exp(z_v - m) (z_v - m),
+      t = z_y if v_begin <= y < v_begin + Vs else -inf.
+    Skipped rows get (-inf, 0, 0, -inf).  Returns float64 [N, 4].
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W_shard = np.asarray(W_shard, dtype=np.float64)
+    n = h.shape[0]
+    Vs = W_shard.shape[0]
+    targets = np.asarray(targets).astype(np.int64)
+    if keep is None:
+        keep = np.ones(n, dtype=np.uint8)
+    out = np.zeros((n, 4))
+    out[:, 0] = -np.inf
+    out[:, 3] = -np.inf
+    idx = np.flatnonzero(np.asarray(keep))
+    if idx.size == 0:
+        return out
+    z = h[idx] @ W_shard.T
+    m = z.max(axis=1)
+    e = np.exp(z - m[:, None])
+    out[idx, 0] = m
+    out[idx, 1] = e.sum(axis=1)
+    out[idx, 2] = (e * (z - m[:, None])).sum(axis=1)
+    local = targets[idx] - v_begin
+    inside = (local >= 0) & (local < Vs)
+    rows = np.flatnonzero(inside)
+    out[idx[rows], 3] = z[rows, local[rows]]
+    return out
+
+
+def merge_shard_partials(partials, keep=None):
+    """Log-prob, entropy and lse of every row from the shards' partials.
+
+    With M = max_r m_r, S = sum_r s_r e^(m_r - M),
+    U = sum_r e^(m_r - M) (u_r + s_r (m_r - M)):
+      lse = M + log S, logprob = t - lse (t from the shard holding y),
+      entropy = log S - U / S.
+    partials float [R, N, 4]; skipped rows (keep == 0) get 0.
+    """
+    P = np.asarray(partials, dtype=np.float64)
+    R, n, _ = P.shape
+    if keep is None:
+        keep = np.ones(n, dtype=np.uint8)
+    lp = np.zeros(n)
+    ent = np.zeros(n)
+    lse = np.zeros(n)
+    for i in np.flatnonzero(np.asarray(keep)):
+        M = P[:, i, 0].max()
+        w = np.exp(P[:, i, 0] - M)
+        S = (P[:, i, 1] * w).sum()
+        U = (w * (P[:, i, 2] + P[:, i, 1] * (P[:, i, 0] - M))).sum()
+        t = P[:, i, 3].max()
+        lse[i] = M + np.log(S)
+        lp[i] = t - lse[i]
+        ent[i] = np.log(S) - U / S
+    return lp, ent, lse

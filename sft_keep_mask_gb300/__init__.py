@@ -11,11 +11,14 @@ from .lmhead import (  # noqa: F401
     LmheadError,
     lmhead_build_keep_mask,
     lmhead_bwd,
+    lmhead_bwd_shard,
     lmhead_compact,
     lmhead_expand,
     lmhead_fwd,
+    lmhead_fwd_shard,
     lmhead_get_status,
     lmhead_launch_count,
+    lmhead_merge_shards,
     lmhead_profile_enable,
     lmhead_profile_read,
     lmhead_selective_log_softmax_bwd,

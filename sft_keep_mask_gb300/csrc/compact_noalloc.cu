@@ -90,7 +90,7 @@ extern "C" lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64
     return cudaMemsetAsync(d_nk, 0, sizeof(int32_t), s) == cudaSuccess ? LMHEAD_OK
                                                                         : LMHEAD_ECUDA;
   }
-  if (launch_compact(keep, targets, N, V, idx, targets_c, d_nk, counts, d_status, s) !=
+  if (launch_compact(keep, targets, N, V, 0, idx, targets_c, d_nk, counts, d_status, s) !=
       cudaSuccess)
     return LMHEAD_ECUDA;
   return LMHEAD_OK;

@@ -92,15 +92,21 @@ constexpr int kCompactRowsPerBlock = 4096;
 cudaError_t launch_build_keep(const float* c0, const float* c1, const float* c2,
                               const int32_t* offsets, int n_seq, int64_t N, uint8_t* keep,
                               cudaStream_t s);
-cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
-                           int32_t* idx, int32_t* targets_c, int32_t* d_nk, int32_t* counts,
-                           int* status, cudaStream_t s);
+// Targets are checked against [0, V_valid) and stored minus t_offset.
+cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t N,
+                           int64_t V_valid, int64_t t_offset, int32_t* idx, int32_t* targets_c,
+                           int32_t* d_nk, int32_t* counts, int* status, cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
                                const int32_t* d_nk, int chunk_index, int chunk_rows, int H,
                                __nv_bfloat16* hc, cudaStream_t s);
 cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
-                         float* lse_c, cudaStream_t s);
+                         float* lse_c, float4* raw_c, cudaStream_t s);
+cudaError_t launch_merge_shards(const float4* partials, int num_shards, const uint8_t* keep,
+                                int64_t N, int want_entropy, float* lp, float* ent, float* lse,
+                                cudaStream_t s);
+cudaError_t launch_expand4(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk, int64_t N,
+                           const float4* src, float4* dst, cudaStream_t s);
 cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,
                            int64_t N, const float* a_c, const float* b_c, const float* c_c,
                            float* a, float* b, float* c, cudaStream_t s);

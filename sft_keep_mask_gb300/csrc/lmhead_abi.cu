@@ -29,8 +29,8 @@ struct Layout {
   int64_t C = 0;        // rows per chunk (multiple of 256)
   int64_t num_vt = 0;   // 256-wide vocab tiles
   int64_t dz_ld = 0;    // row stride of the dZ chunk buffer (elements)
-  size_t hdr = 0, counts = 0, idx = 0, yc = 0, v0 = 0, v1 = 0, v2 = 0, v3 = 0, hc = 0, part = 0,
-         dz = 0, total = 0;
+  size_t hdr = 0, counts = 0, idx = 0, yc = 0, v0 = 0, v1 = 0, v2 = 0, v3 = 0, p4 = 0, hc = 0,
+         part = 0, dz = 0, total = 0;
 };
 
 Layout make_layout(int64_t N, int H, int V, int chunk_rows) {
@@ -54,6 +54,7 @@ Layout make_layout(int64_t N, int H, int V, int chunk_rows) {
   L.v1 = take(static_cast<size_t>(N) * 4);
   L.v2 = take(static_cast<size_t>(N) * 4);
   L.v3 = take(static_cast<size_t>(N) * 4);
+  L.p4 = take(static_cast<size_t>(N) * 16);
   L.hc = take(static_cast<size_t>(L.C) * H * 2);
   L.part = take(static_cast<size_t>(L.num_vt) * L.C * 16);
   L.dz = take(static_cast<size_t>(L.C) * L.dz_ld * 2);
@@ -70,12 +71,12 @@ T* at(void* ws, size_t off) {
 enum Kind : int {
   kKindBuildKeep = 0, kKindCompact, kKindGatherRows, kKindGemmFwd, kKindMerge, kKindExpand,
   kKindGatherVec, kKindZeroRows, kKindGemmDz, kKindGemmDh, kKindGemmDw, kKindSlsFwd,
-  kKindSlsBwd, kNumKinds
+  kKindSlsBwd, kKindMergeShards, kNumKinds
 };
 const char* kKindNames[kNumKinds] = {"build_keep", "compact",  "gather_rows", "gemm_fwd",
                                      "merge",      "expand",   "gather_vec",  "zero_rows",
                                      "gemm_dz",    "gemm_dh",  "gemm_dw",     "sls_fwd",
-                                     "sls_bwd"};
+                                     "sls_bwd",    "merge_shards"};
 
 std::atomic<int64_t> g_launches{0};
 std::mutex g_prof_mu;
@@ -209,15 +210,15 @@ lmhead_status check_ws(void* ws, size_t ws_bytes, const Layout& L) {
   return LMHEAD_OK;
 }
 
-lmhead_status run_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
-                          int32_t* idx, int32_t* yc, int32_t* d_nk, int32_t* counts, int* status,
-                          cudaStream_t s) {
+lmhead_status run_compact(const uint8_t* keep, const int64_t* targets, int64_t N,
+                          int64_t V_valid, int64_t t_offset, int32_t* idx, int32_t* yc,
+                          int32_t* d_nk, int32_t* counts, int* status, cudaStream_t s) {
   if (N == 0) {
     LM_TRY(cudaMemsetAsync(d_nk, 0, sizeof(int32_t), s));
     return LMHEAD_OK;
   }
   Launch l(kKindCompact, s, 2);
-  LM_TRY(launch_compact(keep, targets, N, V, idx, yc, d_nk, counts, status, s));
+  LM_TRY(launch_compact(keep, targets, N, V_valid, t_offset, idx, yc, d_nk, counts, status, s));
   return LMHEAD_OK;
 }
 
@@ -250,62 +251,21 @@ cudaError_t run_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b_singl
   return launch_tc_gemm<MODE>(a, b_single, p, gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN)), s);
 }
 
-}  // namespace
-
-int device_sm_count() { return device_info().sms; }
-
-}  // namespace lmhead
-
-using namespace lmhead;
-
-extern "C" {
-
-size_t lmhead_workspace_size(int64_t N, int H, int V, int want_entropy, int chunk_rows) {
-  (void)want_entropy;
-  if (N < 0 || H < 1 || V < 1) return 0;
-  return make_layout(N, H, V, chunk_rows).total;
-}
-
-lmhead_status lmhead_build_keep_mask(const float* loss_mask, const float* ce_weight,
-                                     const float* kl_weight, const int32_t* seq_offsets,
-                                     int32_t n_seq, int64_t N, uint8_t* keep,
-                                     lmhead_stream_t stream) {
-  if (N < 0 || n_seq < 0 || seq_offsets == nullptr || keep == nullptr) return LMHEAD_EINVAL;
-  if (N == 0) return LMHEAD_OK;
-  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Launch l(kKindBuildKeep, s);
-  return cuda_status(launch_build_keep(loss_mask, ce_weight, kl_weight, seq_offsets, n_seq, N,
-                                       keep, s));
-}
-
-lmhead_status lmhead_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
-                             int32_t* idx, int32_t* targets_c, int32_t* d_nk, void* workspace,
-                             size_t ws_bytes, lmhead_stream_t stream) {
-  if (N < 0 || V < 1 || targets == nullptr || idx == nullptr || targets_c == nullptr ||
-      d_nk == nullptr)
-    return LMHEAD_EINVAL;
-  const Layout L = make_layout(N, 8, V, 256);
-  const size_t need = L.counts + static_cast<size_t>(round_up((cdiv(N, 4096) + 1) * 4, 256));
-  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return LMHEAD_EINVAL;
-  if (ws_bytes < need) return LMHEAD_EWORKSPACE;
-  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int* status = at<int>(workspace, L.hdr);
-  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
-  return run_compact(keep, targets, N, V, idx, targets_c, d_nk, at<int32_t>(workspace, L.counts),
-                     status, s);
-}
-
-lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* targets,
-                         const uint8_t* keep, int64_t N, int H, int V, int want_entropy,
-                         float* logprob, float* entropy, float* lse, int chunk_rows,
-                         void* workspace, size_t ws_bytes, lmhead_stream_t stream) {
+// Forward over the vocabulary rows held in `weight` ([V, H]).  For the whole
+// vocabulary (partial == nullptr) it writes logprob / entropy / lse; for a
+// shard starting at vocabulary row t_offset it writes the shard's per-row
+// (m, s, u, t) partials instead.  Targets are checked against [0, V_valid).
+lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* targets,
+                       const uint8_t* keep, int64_t N, int H, int V, int want_entropy,
+                       float* logprob, float* entropy, float* lse, float4* partial,
+                       int64_t t_offset, int64_t V_valid, int chunk_rows, void* workspace,
+                       size_t ws_bytes, lmhead_stream_t stream) {
   lmhead_status st = check_sizes(N, H, V);
   if (st != LMHEAD_OK) return st;
-  if (hidden == nullptr || weight == nullptr || targets == nullptr || logprob == nullptr ||
-      lse == nullptr || (want_entropy && entropy == nullptr))
+  if (hidden == nullptr || weight == nullptr || targets == nullptr)
+    return LMHEAD_EINVAL;
+  if (partial == nullptr &&
+      (logprob == nullptr || lse == nullptr || (want_entropy && entropy == nullptr)))
     return LMHEAD_EINVAL;
   if (!aligned16(hidden) || !aligned16(weight)) return LMHEAD_EINVAL;
   const Layout L = make_layout(N, H, V, chunk_rows);
@@ -322,12 +282,13 @@ lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* 
   float* lp_c = at<float>(workspace, L.v0);
   float* ent_c = at<float>(workspace, L.v1);
   float* lse_c = at<float>(workspace, L.v2);
+  float4* raw_c = partial != nullptr ? at<float4>(workspace, L.p4) : nullptr;
   __nv_bfloat16* hc = at<__nv_bfloat16>(workspace, L.hc);
   float4* part = at<float4>(workspace, L.part);
 
   LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
-  st = run_compact(keep, targets, N, V, idx, yc, d_nk, at<int32_t>(workspace, L.counts), status,
-                   s);
+  st = run_compact(keep, targets, N, V_valid, t_offset, idx, yc, d_nk,
+                   at<int32_t>(workspace, L.counts), status, s);
   if (st != LMHEAD_OK) return st;
 
   const bool pair = use_pair();
@@ -363,23 +324,31 @@ lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* 
     {
       Launch l(kKindMerge, s);
       LM_TRY(launch_merge(part, static_cast<int>(L.num_vt), d_nk, static_cast<int>(c),
-                          static_cast<int>(L.C), p.want_entropy, lp_c, ent_c, lse_c, s));
+                          static_cast<int>(L.C), p.want_entropy, lp_c, ent_c, lse_c, raw_c, s));
     }
   }
   {
     Launch l(kKindExpand, s);
-    LM_TRY(launch_expand3(keep, idx, d_nk, N, lp_c, want_entropy ? ent_c : nullptr, lse_c,
-                          logprob, want_entropy ? entropy : nullptr, lse, s));
+    if (partial != nullptr) {
+      LM_TRY(launch_expand4(keep, idx, d_nk, N, raw_c, partial, s));
+    } else {
+      LM_TRY(launch_expand3(keep, idx, d_nk, N, lp_c, want_entropy ? ent_c : nullptr, lse_c,
+                            logprob, want_entropy ? entropy : nullptr, lse, s));
+    }
   }
   return LMHEAD_OK;
 }
 
-lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* targets,
-                         const uint8_t* keep, int64_t N, int H, int V, const float* lse,
-                         const float* entropy, const float* grad_logprob,
-                         const float* grad_entropy, void* dhidden, float* dweight,
-                         int dw_accumulate, int chunk_rows, void* workspace, size_t ws_bytes,
-                         lmhead_stream_t stream) {
+// Backward over the vocabulary rows held in `weight` ([V, H], starting at
+// vocabulary row t_offset; lse and entropy are the whole vocabulary's).
+// dhidden receives this shard's dZ W (the whole hidden gradient when the shard
+// is the whole vocabulary); dweight is the shard's [V, H] gradient.
+lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* targets,
+                       const uint8_t* keep, int64_t N, int H, int V, int64_t t_offset,
+                       int64_t V_valid, const float* lse, const float* entropy,
+                       const float* grad_logprob, const float* grad_entropy, void* dhidden,
+                       float* dweight, int dw_accumulate, int chunk_rows, void* workspace,
+                       size_t ws_bytes, lmhead_stream_t stream) {
   lmhead_status st = check_sizes(N, H, V);
   if (st != LMHEAD_OK) return st;
   if (hidden == nullptr || weight == nullptr || targets == nullptr || lse == nullptr ||
@@ -411,8 +380,8 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
   __nv_bfloat16* dz = at<__nv_bfloat16>(workspace, L.dz);
 
   LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
-  st = run_compact(keep, targets, N, V, idx, yc, d_nk, at<int32_t>(workspace, L.counts), status,
-                   s);
+  st = run_compact(keep, targets, N, V_valid, t_offset, idx, yc, d_nk,
+                   at<int32_t>(workspace, L.counts), status, s);
   if (st != LMHEAD_OK) return st;
   {
     Launch l(kKindGatherVec, s);
@@ -480,6 +449,114 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
     }
   }
   return LMHEAD_OK;
+}
+
+}  // namespace
+
+int device_sm_count() { return device_info().sms; }
+
+}  // namespace lmhead
+
+using namespace lmhead;
+
+extern "C" {
+
+size_t lmhead_workspace_size(int64_t N, int H, int V, int want_entropy, int chunk_rows) {
+  (void)want_entropy;
+  if (N < 0 || H < 1 || V < 1) return 0;
+  return make_layout(N, H, V, chunk_rows).total;
+}
+
+lmhead_status lmhead_build_keep_mask(const float* loss_mask, const float* ce_weight,
+                                     const float* kl_weight, const int32_t* seq_offsets,
+                                     int32_t n_seq, int64_t N, uint8_t* keep,
+                                     lmhead_stream_t stream) {
+  if (N < 0 || n_seq < 0 || seq_offsets == nullptr || keep == nullptr) return LMHEAD_EINVAL;
+  if (N == 0) return LMHEAD_OK;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch l(kKindBuildKeep, s);
+  return cuda_status(launch_build_keep(loss_mask, ce_weight, kl_weight, seq_offsets, n_seq, N,
+                                       keep, s));
+}
+
+lmhead_status lmhead_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
+                             int32_t* idx, int32_t* targets_c, int32_t* d_nk, void* workspace,
+                             size_t ws_bytes, lmhead_stream_t stream) {
+  if (N < 0 || V < 1 || targets == nullptr || idx == nullptr || targets_c == nullptr ||
+      d_nk == nullptr)
+    return LMHEAD_EINVAL;
+  const Layout L = make_layout(N, 8, V, 256);
+  const size_t need = L.counts + static_cast<size_t>(round_up((cdiv(N, 4096) + 1) * 4, 256));
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return LMHEAD_EINVAL;
+  if (ws_bytes < need) return LMHEAD_EWORKSPACE;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(workspace, L.hdr);
+  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  return run_compact(keep, targets, N, V, 0, idx, targets_c, d_nk,
+                     at<int32_t>(workspace, L.counts), status, s);
+}
+
+lmhead_status lmhead_fwd(const void* hidden, const void* weight, const int64_t* targets,
+                         const uint8_t* keep, int64_t N, int H, int V, int want_entropy,
+                         float* logprob, float* entropy, float* lse, int chunk_rows,
+                         void* workspace, size_t ws_bytes, lmhead_stream_t stream) {
+  return fwd_impl(hidden, weight, targets, keep, N, H, V, want_entropy, logprob, entropy, lse,
+                  nullptr, 0, V, chunk_rows, workspace, ws_bytes, stream);
+}
+
+lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* targets,
+                         const uint8_t* keep, int64_t N, int H, int V, const float* lse,
+                         const float* entropy, const float* grad_logprob,
+                         const float* grad_entropy, void* dhidden, float* dweight,
+                         int dw_accumulate, int chunk_rows, void* workspace, size_t ws_bytes,
+                         lmhead_stream_t stream) {
+  return bwd_impl(hidden, weight, targets, keep, N, H, V, 0, V, lse, entropy, grad_logprob,
+                  grad_entropy, dhidden, dweight, dw_accumulate, chunk_rows, workspace, ws_bytes,
+                  stream);
+}
+
+lmhead_status lmhead_fwd_shard(const void* hidden, const void* weight_shard,
+                               const int64_t* targets, const uint8_t* keep, int64_t N, int H,
+                               int V_shard, int64_t v_begin, int64_t V_total, int want_entropy,
+                               float* partials, int chunk_rows, void* workspace,
+                               size_t ws_bytes, lmhead_stream_t stream) {
+  if (partials == nullptr || v_begin < 0 || V_shard < 1 || v_begin + V_shard > V_total)
+    return LMHEAD_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(partials) & 15u) != 0) return LMHEAD_EINVAL;
+  return fwd_impl(hidden, weight_shard, targets, keep, N, H, V_shard, want_entropy, nullptr,
+                  nullptr, nullptr, reinterpret_cast<float4*>(partials), v_begin, V_total,
+                  chunk_rows, workspace, ws_bytes, stream);
+}
+
+lmhead_status lmhead_merge_shards(const float* partials, int num_shards, const uint8_t* keep,
+                                  int64_t N, int want_entropy, float* logprob, float* entropy,
+                                  float* lse, lmhead_stream_t stream) {
+  if (N < 0 || num_shards < 1 || partials == nullptr || logprob == nullptr || lse == nullptr ||
+      (want_entropy && entropy == nullptr) || (reinterpret_cast<uintptr_t>(partials) & 15u) != 0)
+    return LMHEAD_EINVAL;
+  if (N == 0) return LMHEAD_OK;
+  if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch l(kKindMergeShards, s);
+  return cuda_status(launch_merge_shards(reinterpret_cast<const float4*>(partials), num_shards,
+                                         keep, N, want_entropy ? 1 : 0, logprob,
+                                         want_entropy ? entropy : nullptr, lse, s));
+}
+
+lmhead_status lmhead_bwd_shard(const void* hidden, const void* weight_shard,
+                               const int64_t* targets, const uint8_t* keep, int64_t N, int H,
+                               int V_shard, int64_t v_begin, int64_t V_total, const float* lse,
+                               const float* entropy, const float* grad_logprob,
+                               const float* grad_entropy, void* dhidden_partial,
+                               float* dweight_shard, int dw_accumulate, int chunk_rows,
+                               void* workspace, size_t ws_bytes, lmhead_stream_t stream) {
+  if (v_begin < 0 || V_shard < 1 || v_begin + V_shard > V_total) return LMHEAD_EINVAL;
+  return bwd_impl(hidden, weight_shard, targets, keep, N, H, V_shard, v_begin, V_total, lse,
+                  entropy, grad_logprob, grad_entropy, dhidden_partial, dweight_shard,
+                  dw_accumulate, chunk_rows, workspace, ws_bytes, stream);
 }
 
 lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,

@@ -77,10 +77,13 @@ __global__ void count_kernel(const uint8_t* __restrict__ keep, int64_t N, int32_
 
 // Writes the kept rows of block b, in order, after the kept rows of blocks
 // 0..b-1; the last block also writes Nk.
+// Targets are checked against [0, V_valid) and stored relative to t_offset
+// (the first vocabulary row of a shard; 0 for the whole vocabulary).
 __global__ void scatter_kernel(const uint8_t* __restrict__ keep,
-                               const int64_t* __restrict__ targets, int64_t N, int V,
-                               const int32_t* __restrict__ counts, int32_t* __restrict__ idx,
-                               int32_t* __restrict__ targets_c, int32_t* d_nk, int* status) {
+                               const int64_t* __restrict__ targets, int64_t N, int64_t V_valid,
+                               int64_t t_offset, const int32_t* __restrict__ counts,
+                               int32_t* __restrict__ idx, int32_t* __restrict__ targets_c,
+                               int32_t* d_nk, int* status) {
   __shared__ int red[kScanThreads / 32];
   __shared__ int warp_tot[kScanThreads / 32];
   // offset of this block = sum of the counts of the blocks before it
@@ -112,12 +115,12 @@ __global__ void scatter_kernel(const uint8_t* __restrict__ keep,
     if (bits & (1u << j)) {
       const int64_t r = base + j;
       int64_t y = targets[r];
-      if (y < 0 || y >= V) {
+      if (y < 0 || y >= V_valid) {
         atomicCAS(status, 0, kStatusTarget);
         y = 0;
       }
       idx[pos] = static_cast<int32_t>(r);
-      targets_c[pos] = static_cast<int32_t>(y);
+      targets_c[pos] = static_cast<int32_t>(y - t_offset);
       ++pos;
     }
   }
@@ -170,7 +173,7 @@ __global__ void gather_vec_kernel(const int32_t* __restrict__ idx, const int32_t
 __global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const int32_t* d_nk,
                              int chunk_index, int chunk_rows, int want_entropy,
                              float* __restrict__ lp_c, float* __restrict__ ent_c,
-                             float* __restrict__ lse_c) {
+                             float* __restrict__ lse_c, float4* __restrict__ raw_c) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
@@ -185,11 +188,55 @@ __global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const 
     U = fmaf(sc, fmaf(q.y, q.x - M, q.z), U);
     T = fmaxf(T, q.w);
   }
+  if (raw_c != nullptr) {  // a vocabulary shard: keep the unnormalised reduction
+    raw_c[chunk_start + r] = make_float4(M, S, U, T);
+    return;
+  }
   const float logS = logf(S);
   const float lse = M + logS;
   lp_c[chunk_start + r] = T - lse;
   lse_c[chunk_start + r] = lse;
   if (want_entropy) ent_c[chunk_start + r] = logS - U / S;
+}
+
+// Merge of the vocabulary shards' (m, s, u, t) partials, [S][N] float4, into
+// logprob, entropy and lse of every row (skipped rows get +0.0).
+__global__ void merge_shards_kernel(const float4* __restrict__ partials, int num_shards,
+                                    const uint8_t* __restrict__ keep, int64_t N,
+                                    int want_entropy, float* __restrict__ lp,
+                                    float* __restrict__ ent, float* __restrict__ lse) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  if (keep != nullptr && keep[i] == 0) {
+    lp[i] = 0.f;
+    lse[i] = 0.f;
+    if (ent) ent[i] = 0.f;
+    return;
+  }
+  float M = -INFINITY;
+  for (int r = 0; r < num_shards; ++r) M = fmaxf(M, partials[r * N + i].x);
+  float S = 0.f, U = 0.f, T = -INFINITY;
+  for (int r = 0; r < num_shards; ++r) {
+    const float4 q = partials[r * N + i];
+    const float sc = expf(q.x - M);
+    S = fmaf(q.y, sc, S);
+    U = fmaf(sc, fmaf(q.y, q.x - M, q.z), U);
+    T = fmaxf(T, q.w);
+  }
+  const float logS = logf(S);
+  lse[i] = M + logS;
+  lp[i] = T - (M + logS);
+  if (want_entropy) ent[i] = logS - U / S;
+}
+
+// Expand compact float4 rows to all rows; skipped rows get (-inf, 0, 0, -inf).
+__global__ void expand4_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ idx,
+                               const int32_t* d_nk, int64_t N, const float4* __restrict__ src,
+                               float4* __restrict__ dst) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  if (keep != nullptr && keep[i] == 0) dst[i] = make_float4(-INFINITY, 0.f, 0.f, -INFINITY);
+  if (i < *d_nk) dst[idx[i]] = src[i];
 }
 
 // ------------------------------------------------------------------- expand
@@ -242,15 +289,15 @@ cudaError_t launch_build_keep(const float* c0, const float* c1, const float* c2,
   return cudaGetLastError();
 }
 
-cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t N, int V,
-                           int32_t* idx, int32_t* targets_c, int32_t* d_nk, int32_t* counts,
-                           int* status, cudaStream_t s) {
+cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t N,
+                           int64_t V_valid, int64_t t_offset, int32_t* idx, int32_t* targets_c,
+                           int32_t* d_nk, int32_t* counts, int* status, cudaStream_t s) {
   const unsigned nb = blocks_for(N, kScanTile);
   count_kernel<<<nb, kScanThreads, 0, s>>>(keep, N, counts);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  scatter_kernel<<<nb, kScanThreads, 0, s>>>(keep, targets, N, V, counts, idx, targets_c, d_nk,
-                                             status);
+  scatter_kernel<<<nb, kScanThreads, 0, s>>>(keep, targets, N, V_valid, t_offset, counts, idx,
+                                             targets_c, d_nk, status);
   return cudaGetLastError();
 }
 
@@ -266,10 +313,24 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
 
 cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
-                         float* lse_c, cudaStream_t s) {
+                         float* lse_c, float4* raw_c, cudaStream_t s) {
   merge_kernel<<<blocks_for(chunk_rows, 128), 128, 0, s>>>(part, num_vt, d_nk, chunk_index,
                                                            chunk_rows, want_entropy, lp_c, ent_c,
-                                                           lse_c);
+                                                           lse_c, raw_c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_shards(const float4* partials, int num_shards, const uint8_t* keep,
+                                int64_t N, int want_entropy, float* lp, float* ent, float* lse,
+                                cudaStream_t s) {
+  merge_shards_kernel<<<blocks_for(N, 256), 256, 0, s>>>(partials, num_shards, keep, N,
+                                                         want_entropy, lp, ent, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand4(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk, int64_t N,
+                           const float4* src, float4* dst, cudaStream_t s) {
+  expand4_kernel<<<blocks_for(N, 256), 256, 0, s>>>(keep, idx, d_nk, N, src, dst);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,11 @@ _SIGS = {
     "lmhead_bwd": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                           _I32, _I32, _VP, ctypes.c_size_t, _VP]),
     "lmhead_expand": (_I32, [_VP, _VP, _VP, _I64, _VP, _VP]),
+    "lmhead_fwd_shard": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I64, _I64, _I32, _VP, _I32,
+                                _VP, ctypes.c_size_t, _VP]),
+    "lmhead_merge_shards": (_I32, [_VP, _I32, _VP, _I64, _I32, _VP, _VP, _VP, _VP]),
+    "lmhead_bwd_shard": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I64, _I64, _VP, _VP, _VP,
+                                _VP, _VP, _VP, _I32, _I32, _VP, ctypes.c_size_t, _VP]),
     "lmhead_selective_log_softmax_fwd": (_I32, [_VP, _I32, _I64, _VP, _VP, _I64, _I32, _I32, _VP,
                                                 _VP, _VP, _VP, _VP]),
     "lmhead_selective_log_softmax_bwd": (_I32, [_VP, _I32, _I64, _VP, _VP, _I64, _I32, _VP, _VP,
@@ -180,6 +185,59 @@ def lmhead_bwd(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_e
                             _p(dweight), int(bool(dw_accumulate)), int(chunk_rows),
                             _p(workspace), workspace.numel(), _s(stream))
     _check(code, "lmhead_bwd")
+
+
+def lmhead_fwd_shard(hidden, weight_shard, v_begin, V_total, targets, keep, want_entropy,
+                     partials, workspace, chunk_rows=0, stream=None):
+    N, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight_shard, torch.bfloat16, "weight_shard", Vs * H)
+    _need(targets, torch.int64, "targets", N)
+    _need(keep, torch.uint8, "keep", N)
+    _need(partials, torch.float32, "partials", N * 4)
+    _need(workspace, torch.uint8, "workspace")
+    code = lib().lmhead_fwd_shard(_p(hidden), _p(weight_shard), _p(targets), _p(keep), N, H, Vs,
+                                  int(v_begin), int(V_total), int(bool(want_entropy)),
+                                  _p(partials), int(chunk_rows), _p(workspace),
+                                  workspace.numel(), _s(stream))
+    _check(code, "lmhead_fwd_shard")
+
+
+def lmhead_merge_shards(partials, keep, want_entropy, logprob, entropy, lse, stream=None):
+    S, N = partials.shape[0], partials.shape[1]
+    _need(partials, torch.float32, "partials", S * N * 4)
+    _need(keep, torch.uint8, "keep", N)
+    _need(logprob, torch.float32, "logprob", N)
+    _need(entropy, torch.float32, "entropy", N)
+    _need(lse, torch.float32, "lse", N)
+    code = lib().lmhead_merge_shards(_p(partials), S, _p(keep), N, int(bool(want_entropy)),
+                                     _p(logprob), _p(entropy), _p(lse), _s(stream))
+    _check(code, "lmhead_merge_shards")
+
+
+def lmhead_bwd_shard(hidden, weight_shard, v_begin, V_total, targets, keep, lse, entropy,
+                     grad_logprob, grad_entropy, dhidden_partial, dweight_shard, dw_accumulate,
+                     workspace, chunk_rows=0, stream=None):
+    N, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight_shard, torch.bfloat16, "weight_shard", Vs * H)
+    _need(targets, torch.int64, "targets", N)
+    _need(keep, torch.uint8, "keep", N)
+    _need(lse, torch.float32, "lse", N)
+    _need(entropy, torch.float32, "entropy", N)
+    _need(grad_logprob, torch.float32, "grad_logprob", N)
+    _need(grad_entropy, torch.float32, "grad_entropy", N)
+    _need(dhidden_partial, torch.bfloat16, "dhidden_partial", N * H)
+    _need(dweight_shard, torch.float32, "dweight_shard", Vs * H)
+    _need(workspace, torch.uint8, "workspace")
+    code = lib().lmhead_bwd_shard(_p(hidden), _p(weight_shard), _p(targets), _p(keep), N, H, Vs,
+                                  int(v_begin), int(V_total), _p(lse), _p(entropy),
+                                  _p(grad_logprob), _p(grad_entropy), _p(dhidden_partial),
+                                  _p(dweight_shard), int(bool(dw_accumulate)), int(chunk_rows),
+                                  _p(workspace), workspace.numel(), _s(stream))
+    _check(code, "lmhead_bwd_shard")
 
 
 def lmhead_expand(src, idx, d_nk, N, dst, stream=None):

@@ -63,7 +63,7 @@ def test_workspace_size_formula(L):
     # chunk buffers: dz [C, V] bf16 + h_c [C, H] bf16 + partials [V/256, C] x 16 B
     C = 8192
     core = C * V * 2 + C * H * 2 + (V // 256 + 1) * C * 16
-    assert core <= a <= core + 65536 * 4 * 8 + 4096
+    assert core <= a <= core + 65536 * 48 + 4096
 
 
 def _fake(addr=1 << 20):

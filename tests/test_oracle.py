@@ -445,3 +445,43 @@ def test_sls_backward_finite_differences(with_entropy):
     assert np.linalg.norm(dz - num) <= 1e-7 * max(np.linalg.norm(num), 1.0)
     np.testing.assert_allclose(dz.sum(axis=1), 0.0, atol=1e-12)
     assert not dz[2].any()
+
+
+# --------------------------------------------- vocabulary-parallel shards
+
+def test_shard_merge_equals_full_forward():
+    # splitting the vocabulary into shards and merging their partials gives
+    # the forward of the whole vocabulary (any split, uneven shards)
+    h, W, y, keep, _, _ = _problem(60, 40, 16, 101, scale=3.0)
+    full = O.forward(h, W, y, keep)
+    for bounds in ([0, 101], [0, 50, 101], [0, 7, 8, 64, 101]):
+        parts = np.stack([O.shard_partials(h, W[a:b], a, y, keep)
+                          for a, b in zip(bounds[:-1], bounds[1:])])
+        got = O.merge_shard_partials(parts, keep)
+        for g, f in zip(got, full):
+            np.testing.assert_allclose(g, f, atol=1e-12)
+
+
+def test_shard_partials_closed_form():
+    # a shard of W = 0 has z = 0: m = 0, s = Vs, u = 0; t = 0 iff y inside
+    h = np.ones((3, 4))
+    y = np.array([2, 9, 15])
+    P = O.shard_partials(h, np.zeros((6, 4)), 8, y)
+    np.testing.assert_allclose(P[:, 0], 0.0)
+    np.testing.assert_allclose(P[:, 1], 6.0)
+    np.testing.assert_allclose(P[:, 2], 0.0)
+    assert P[0, 3] == -np.inf and P[1, 3] == 0.0 and P[2, 3] == -np.inf
+
+
+def test_shard_backward_sums_to_full_backward():
+    # dz of a shard uses the global lse / entropy; the hidden gradient is the
+    # sum over shards of dz_shard @ W_shard, dW is the concatenation
+    h, W, y, keep, g_lp, g_ent = _problem(61, 30, 12, 77)
+    dh, dW = O.backward(h, W, y, keep, g_lp, g_ent)
+    z = h @ W.T
+    dz = O.selective_log_softmax_backward(z, y, keep, g_lp, g_ent)
+    dh_sum = np.zeros_like(dh)
+    for a, b in ((0, 30), (30, 77)):
+        dh_sum += dz[:, a:b] @ W[a:b]
+        np.testing.assert_allclose(dz[:, a:b].T @ h, dW[a:b], atol=1e-12)
+    np.testing.assert_allclose(dh_sum, dh, atol=1e-12)
