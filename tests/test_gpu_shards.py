@@ -73,5 +73,6 @@ def test_shard_arguments_are_checked():
     sc = LMHeadScorer(64, 64, 500)
     parts = torch.empty(64, 4, device=DEV)
     with pytest.raises(L.LmheadError):
-        L.lmhead_fwd_shard(inp["hidden"], inp["weight"][600:].contiguous(), 600, 1000,
+        # a 400-row shard starting at 700 runs past V_total = 1000
+        L.lmhead_fwd_shard(inp["hidden"], inp["weight"][600:].contiguous(), 700, 1000,
                            inp["targets"], None, True, parts, sc.workspace)
