@@ -50,6 +50,9 @@ struct TcGemmParams {
   __nv_bfloat16* dhidden;   // kDh: [N, H]
   float* dw;                // kDw: [V, H]
   int beta;                 // kDw: 1 = add to dw
+  float* dh_part;           // kDh split over K: [max_split][C][H] fp32 partial sums
+  int max_split;            // kDh: largest K split (1 = never split)
+  int split_fill_pct;       // kDh: split only below this fill of the worker slots
 };
 
 template <int MODE>
@@ -85,6 +88,32 @@ __device__ __forceinline__ void chunk_span(int nk, int C, int c, int& start, int
   rows = nk - start < cb ? nk - start : cb;
 }
 
+// Number of K splits of the dHidden contraction (K = V is long, the tile grid
+// is small).  Unsplit, the last wave of `workers` persistent CTAs (or CTA
+// pairs) is partly idle; measured on GB300, that tail costs less than its
+// share of tiles (the few workers left run faster), so the contraction is split
+// only when fewer than 85% of the worker-slots hold a tile -- then into the
+// S <= max_split that fills the slots best (the smallest S among equals).
+// With S > 1 the contraction writes fp32 partials that a reduction adds up.
+__host__ __device__ __forceinline__ int dh_split_count(int tiles, int workers, int num_kb,
+                                                      int max_split, int min_fill_pct = 85) {
+  if (tiles <= 0 || workers <= 0) return 1;
+  int best = 1;
+  long long best_num = tiles, best_den = (long long)((tiles + workers - 1) / workers) * workers;
+  if (best_num * 100 >= best_den * min_fill_pct) return 1;
+  for (int s = 2; s <= max_split && s <= num_kb; ++s) {
+    const long long units = (long long)tiles * s;
+    const long long den = (units + workers - 1) / workers * workers;
+    // strictly better by at least 1% of a wave's worth of efficiency
+    if (units * best_den > best_num * den + den * best_den / 100) {
+      best = s;
+      best_num = units;
+      best_den = den;
+    }
+  }
+  return best;
+}
+
 // Rows counted by one block of the compaction scan (rowops.cu).
 constexpr int kCompactRowsPerBlock = 4096;
 
@@ -115,6 +144,12 @@ cudaError_t launch_expand(const float* src, const int32_t* idx, const int32_t* d
 cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N,
                               const float* a, const float* b, const float* c, const float* d,
                               float* a_c, float* b_c, float* c_c, float* d_c, cudaStream_t s);
+// Sum of the dHidden K-split partials of one chunk, rows scattered to
+// dhidden[idx] as bf16; does nothing when the contraction was not split.
+cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
+                             int chunk_rows, int H, int tile_m, int workers, int num_kb,
+                             int max_split, int fill_pct, const int32_t* idx,
+                             __nv_bfloat16* dhidden, cudaStream_t s);
 cudaError_t launch_zero_skipped_rows(const uint8_t* keep, int64_t N, int H,
                                      __nv_bfloat16* dhidden, cudaStream_t s);
 

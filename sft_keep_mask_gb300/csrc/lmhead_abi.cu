@@ -19,6 +19,9 @@ namespace lmhead {
 namespace {
 
 constexpr bool kDefaultPair = true;
+constexpr int kDhMaxSplit = 4;  // largest K split of the dHidden contraction
+static_assert(kDhMaxSplit <= 4, "the dHidden reduction sums at most four partials");
+constexpr int kDhSplitFillPct = 85;  // split only when fewer worker slots than this are busy
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 inline int64_t cdiv(int64_t x, int64_t m) { return (x + m - 1) / m; }
@@ -30,7 +33,7 @@ struct Layout {
   int64_t num_vt = 0;   // 256-wide vocab tiles
   int64_t dz_ld = 0;    // row stride of the dZ chunk buffer (elements)
   size_t hdr = 0, counts = 0, idx = 0, yc = 0, v0 = 0, v1 = 0, v2 = 0, v3 = 0, p4 = 0, hc = 0,
-         part = 0, dz = 0, total = 0;
+         part = 0, dz = 0, dhp = 0, total = 0;
 };
 
 Layout make_layout(int64_t N, int H, int V, int chunk_rows) {
@@ -58,6 +61,7 @@ Layout make_layout(int64_t N, int H, int V, int chunk_rows) {
   L.hc = take(static_cast<size_t>(L.C) * H * 2);
   L.part = take(static_cast<size_t>(L.num_vt) * L.C * 16);
   L.dz = take(static_cast<size_t>(L.C) * L.dz_ld * 2);
+  L.dhp = take(static_cast<size_t>(kDhMaxSplit) * L.C * H * 4);
   L.total = off;
   return L;
 }
@@ -71,12 +75,12 @@ T* at(void* ws, size_t off) {
 enum Kind : int {
   kKindBuildKeep = 0, kKindCompact, kKindGatherRows, kKindGemmFwd, kKindMerge, kKindExpand,
   kKindGatherVec, kKindZeroRows, kKindGemmDz, kKindGemmDh, kKindGemmDw, kKindSlsFwd,
-  kKindSlsBwd, kKindMergeShards, kNumKinds
+  kKindSlsBwd, kKindMergeShards, kKindDhReduce, kNumKinds
 };
 const char* kKindNames[kNumKinds] = {"build_keep", "compact",  "gather_rows", "gemm_fwd",
                                      "merge",      "expand",   "gather_vec",  "zero_rows",
                                      "gemm_dz",    "gemm_dh",  "gemm_dw",     "sls_fwd",
-                                     "sls_bwd",    "merge_shards"};
+                                     "sls_bwd",    "merge_shards", "dh_reduce"};
 
 std::atomic<int64_t> g_launches{0};
 std::mutex g_prof_mu;
@@ -238,17 +242,23 @@ bool use_pair() {
 // Launches one contraction on the selected variant.  m_upper bounds the rows
 // of D (the chunk for kFwd/kDz/kDh, V for kDw); b_single / b_pair are the B
 // maps for the two variants (they differ only for K-major B).
+// *workers receives the number of persistent workers launched (CTA pairs or
+// CTAs), which the dHidden split rule depends on.
 template <int MODE>
 cudaError_t run_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b_single,
                      const CUtensorMap& b_pair, const TcGemmParams& p, int64_t m_upper,
-                     int64_t n, cudaStream_t s) {
+                     int64_t n, cudaStream_t s, int* workers = nullptr) {
+  const int split = MODE == kDh ? p.max_split : 1;
   if (pair) {
-    const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, kBN);
+    const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, kBN) * split;
     const int64_t pairs = device_info().sms / 2;
-    const int grid = static_cast<int>(2 * (tiles < pairs ? (tiles < 1 ? 1 : tiles) : pairs));
-    return launch_tc_gemm_pair<MODE>(a, b_pair, p, grid, s);
+    const int64_t w = tiles < pairs ? (tiles < 1 ? 1 : tiles) : pairs;
+    if (workers != nullptr) *workers = static_cast<int>(w);
+    return launch_tc_gemm_pair<MODE>(a, b_pair, p, static_cast<int>(2 * w), s);
   }
-  return launch_tc_gemm<MODE>(a, b_single, p, gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN)), s);
+  const int grid = gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN) * split);
+  if (workers != nullptr) *workers = grid;
+  return launch_tc_gemm<MODE>(a, b_single, p, grid, s);
 }
 
 // Forward over the vocabulary rows held in `weight` ([V, H]).  For the whole
@@ -421,6 +431,10 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.dz_ld = L.dz_ld;
   p.dhidden = static_cast<__nv_bfloat16*>(dhidden);
   p.dw = dweight;
+  p.dh_part = at<float>(workspace, L.dhp);
+  p.max_split = kDhMaxSplit;
+  p.split_fill_pct = kDhSplitFillPct;
+  int dh_workers = 0;
   const int64_t n_h_tiles = cdiv(H, kBN);
 
   const int64_t max_chunks = cdiv(N, L.C);
@@ -439,7 +453,14 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     {
       Launch l(kKindGemmDh, s);
       p.group_n = static_cast<int>(n_h_tiles);
-      LM_TRY(run_gemm<kDh>(pair, m_dz_k, m_w_mn, m_w_mn, p, L.C, H, s));
+      LM_TRY(run_gemm<kDh>(pair, m_dz_k, m_w_mn, m_w_mn, p, L.C, H, s, &dh_workers));
+    }
+    {
+      Launch l(kKindDhReduce, s);
+      LM_TRY(launch_dh_reduce(p.dh_part, d_nk, static_cast<int>(c), static_cast<int>(L.C), H,
+                              pair ? 256 : kBM, dh_workers, static_cast<int>(cdiv(V, kBK)),
+                              p.max_split, p.split_fill_pct, idx,
+                              static_cast<__nv_bfloat16*>(dhidden), s));
     }
     {
       Launch l(kKindGemmDw, s);

@@ -266,6 +266,41 @@ __global__ void scatter_vals_kernel(const float* __restrict__ src, const int32_t
   if (k < *d_nk) dst[idx[k]] = src[k];
 }
 
+__global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t* d_nk,
+                                 int chunk_index, int chunk_rows, int H, int tile_m, int workers,
+                                 int num_kb, int max_split, int fill_pct,
+                                 const int32_t* __restrict__ idx, uint2* __restrict__ dhidden) {
+  int chunk_start, rows;
+  chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
+  if (rows == 0) return;
+  const int tiles = ((rows + tile_m - 1) / tile_m) * ((H + 255) / 256);
+  const int splits = dh_split_count(tiles, workers, num_kb, max_split, fill_pct);
+  if (splits == 1) return;
+  const int q = H / 4;  // float4 columns per row
+  const int64_t plane = static_cast<int64_t>(chunk_rows) * q;
+  const int64_t total = static_cast<int64_t>(rows) * q;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(g / q);
+    const int c = static_cast<int>(g - static_cast<int64_t>(r) * q);
+    const int64_t at = static_cast<int64_t>(r) * q + c;
+    // all partial loads in flight before the (fixed-order) sum
+    float4 v[4];
+#pragma unroll
+    for (int sidx = 0; sidx < 4; ++sidx)
+      v[sidx] = sidx < splits ? __ldcs(part + sidx * plane + at) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = v[0];
+#pragma unroll
+    for (int sidx = 1; sidx < 4; ++sidx) {
+      if (sidx < splits) {
+        acc.x += v[sidx].x; acc.y += v[sidx].y; acc.z += v[sidx].z; acc.w += v[sidx].w;
+      }
+    }
+    const int64_t orow = idx[chunk_start + r];
+    dhidden[orow * q + c] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+}
+
 // Rows of skipped tokens of dhidden are written as zeros (warp per row).
 __global__ void zero_skipped_rows_kernel(const uint8_t* __restrict__ keep, int64_t N,
                                          int vec_per_row, uint4* __restrict__ dh) {
@@ -353,6 +388,21 @@ cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N
                               const float* b, const float* c, const float* d, float* a_c,
                               float* b_c, float* c_c, float* d_c, cudaStream_t s) {
   gather_vec_kernel<<<blocks_for(N, 256), 256, 0, s>>>(idx, d_nk, a, b, c, d, a_c, b_c, c_c, d_c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
+                             int chunk_rows, int H, int tile_m, int workers, int num_kb,
+                             int max_split, int fill_pct, const int32_t* idx,
+                             __nv_bfloat16* dhidden, cudaStream_t s) {
+  // a grid-stride loop over a grid of 4 blocks per SM: cheap when the
+  // contraction was not split and the kernel returns at once
+  const int64_t threads = static_cast<int64_t>(chunk_rows) * (H / 4);
+  const unsigned want = blocks_for(threads, 256);
+  const unsigned cap = static_cast<unsigned>(4 * (device_sm_count() > 0 ? device_sm_count() : 148));
+  dh_reduce_kernel<<<want < cap ? want : cap, 256, 0, s>>>(
+      reinterpret_cast<const float4*>(part), d_nk, chunk_index, chunk_rows, H, tile_m, workers,
+      num_kb, max_split, fill_pct, idx, reinterpret_cast<uint2*>(dhidden));
   return cudaGetLastError();
 }
 

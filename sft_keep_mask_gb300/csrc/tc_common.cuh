@@ -61,11 +61,12 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 //   cstart     first compact row of the chunk
 //   rows_valid rows of the chunk that hold kept tokens
 //   have_acc   false only for kDw with an empty K range (writes zeros)
+//   split_idx, splits  kDh with its K range split: write fp32 partial sums
 //   release    called once, right after the last TMEM load of the tile
 template <int MODE, typename Release>
 __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tbase, int row,
                                               int nt, int cstart, int rows_valid, bool have_acc,
-                                              Release&& release) {
+                                              int split_idx, int splits, Release&& release) {
   constexpr int kSlices = kBN / 32;
   const int col_tile = nt * kBN;
 
@@ -194,6 +195,8 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
     const bool row_ok = row < rows_valid;
     const int64_t orow = row_ok ? p.idx[cstart + row] : 0;
     __nv_bfloat16* hrow = p.dhidden + orow * p.H;
+    float* prow = p.dh_part +
+                  (static_cast<int64_t>(split_idx) * p.chunk_rows + (row_ok ? row : 0)) * p.H;
 #pragma unroll 1
     for (int c = 0; c < kSlices; ++c) {
       uint32_t r[32];
@@ -203,6 +206,15 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
       if (c == kSlices - 1) release();
       const int col = col_tile + c * 32;
       if (!row_ok || col >= p.H) continue;
+      if (splits > 1) {
+        float4* dst = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          if (col + 4 * v < p.H)
+            dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        continue;
+      }
       uint4* dst = reinterpret_cast<uint4*>(hrow + col);
 #pragma unroll
       for (int v = 0; v < 4; ++v) {

@@ -60,7 +60,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_n = (N + kBN - 1) / kBN;
   const int num_kb = (K + kBK - 1) / kBK;
   const int num_tiles = num_m * num_n;
-  if (static_cast<int>(blockIdx.x) >= num_tiles) return;
+  const int splits = MODE == kDh ? dh_split_count(num_tiles, static_cast<int>(gridDim.x), num_kb, p.max_split, p.split_fill_pct) : 1;
+  const int num_units = num_tiles * splits;
+  if (static_cast<int>(blockIdx.x) >= num_units) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -94,11 +96,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const int t = u % num_tiles;
+        const int sidx = u / num_tiles;
+        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
         int mt, nt;
         tile_coords(t, num_m, num_n, p.group_n, mt, nt);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
           uint8_t* a_dst = sA + stage * kABytes;
@@ -141,13 +147,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok && num_kb > 0; t += gridDim.x, ++it) {
+      for (int u = blockIdx.x; u < num_units && ok && num_kb > 0; u += gridDim.x, ++it) {
+        const int t = u % num_tiles;
+        const int sidx = u / num_tiles;
+        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
+
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_addr(sA + stage * kABytes);
@@ -158,7 +169,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                      : smem_desc_sw128(a_addr + k * 32, 16, 1024);
             const uint64_t bd = b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                      : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -177,7 +188,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row_local = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+      const int t = u % num_tiles;
+      const int sidx = u / num_tiles;
       int mt, nt;
       tile_coords(t, num_m, num_n, p.group_n, mt, nt);
       const int acc = it & 1;
@@ -188,7 +201,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
       uint64_t* te = &tempty[acc];
-      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, cstart, rows_valid, num_kb > 0, [&] {
+      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, cstart, rows_valid, num_kb > 0, sidx, splits, [&] {
         tc_fence_before();
         mbar_arrive(te);
       });

@@ -59,7 +59,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int num_n = (N + kBN - 1) / kBN;
   const int num_kb = (K + kBK - 1) / kBK;
   const int num_tiles = num_m * num_n;
-  if (pair >= num_tiles) return;  // both CTAs of the pair leave together
+  const int splits = MODE == kDh ? dh_split_count(num_tiles, num_pairs, num_kb, p.max_split, p.split_fill_pct) : 1;
+  const int num_units = num_tiles * splits;
+  if (pair >= num_units) return;  // both CTAs of the pair leave together
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
@@ -97,11 +99,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_a = make_l2_policy(p.hint_a);
       const uint64_t pol_b = make_l2_policy(p.hint_b);
       const bool ha = p.hint_a != 0, hb = p.hint_b != 0;
-      for (int t = pair; t < num_tiles; t += num_pairs) {
+      for (int u = pair; u < num_units; u += num_pairs) {
+        const int t = u % num_tiles;
+        const int sidx = u / num_tiles;
+        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
         int mt, nt;
         tile_coords(t, num_m, num_n, p.group_n, mt, nt);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPairABytes + kPairBBytes));
           const uint32_t bar = map_to_cta(smem_addr(&full[stage]), 0);
@@ -148,13 +154,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok && num_kb > 0; t += num_pairs, ++it) {
+      for (int u = pair; u < num_units && ok && num_kb > 0; u += num_pairs, ++it) {
+        const int t = u % num_tiles;
+        const int sidx = u / num_tiles;
+        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
+
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_addr(sA + stage * kPairABytes);
@@ -165,7 +176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                      : smem_desc_sw128(a_addr + k * 32, 16, 1024);
             const uint64_t bd = b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                      : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           umma_commit_pair(&empty[stage], 0x3);
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
@@ -183,7 +194,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int row_local = static_cast<int>(rank) * 128 + q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
-    for (int t = pair; t < num_tiles; t += num_pairs, ++it) {
+    for (int u = pair; u < num_units; u += num_pairs, ++it) {
+      const int t = u % num_tiles;
+      const int sidx = u / num_tiles;
       int mt, nt;
       tile_coords(t, num_m, num_n, p.group_n, mt, nt);
       const int acc = it & 1;
@@ -194,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
       const uint32_t te = map_to_cta(smem_addr(&tempty[acc]), 0);
-      epilogue_tile<MODE>(p, tbase, mt * kPairTileM + row_local, nt, cstart, rows_valid, num_kb > 0,
+      epilogue_tile<MODE>(p, tbase, mt * kPairTileM + row_local, nt, cstart, rows_valid, num_kb > 0, sidx, splits,
                           [&] {
                             tc_fence_before();
                             __syncwarp();
