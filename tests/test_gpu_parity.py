@@ -317,3 +317,18 @@ def test_chunk_boundaries(nk):
     keep = np.zeros(w.N, np.uint8)
     keep[np.random.default_rng(nk).choice(w.N, nk, replace=False)] = 1
     _run_both(w, keep_override=keep, chunk_rows=256)
+
+
+@pytest.mark.parametrize("variant", ["pair", "single"])
+@pytest.mark.parametrize("N,H,V", [(1, 8, 1), (5, 16, 2), (33, 64, 7), (300, 8, 300),
+                                   (70, 24, 129)])
+def test_tiny_and_degenerate_shapes(monkeypatch, variant, N, H, V):
+    # shapes smaller than one tile in every dimension: TMA boxes reach past the
+    # tensor (zero fill), V = 1 makes every logprob and entropy exactly 0
+    monkeypatch.setenv("LMHEAD_GEMM", variant)
+    w = synth.workload("tiny", seed=90 + N + V, N=N, H=H, V=V)
+    _run_both(w, keep_override=np.ones(N, np.uint8))
+    if N > 1:
+        keep = np.zeros(N, np.uint8)
+        keep[::2] = 1
+        _run_both(w, keep_override=keep)
