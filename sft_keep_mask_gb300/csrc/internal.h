@@ -53,6 +53,8 @@ struct TcGemmParams {
   float* dh_part;           // kDh split over K: [max_split][C][H] fp32 partial sums
   int max_split;            // kDh: largest K split (1 = never split)
   int split_fill_pct;       // kDh: split only below this fill of the worker slots
+  int stall;                // fault injection: the producer issues no loads, so
+                            //   the pipeline waits run out (device ETIMEOUT)
 };
 
 template <int MODE>

@@ -153,8 +153,19 @@ EncodeTiledFn encode_fn() {
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
 // `ld` elements; boxes of [box_rows, box_cols] with the 128-byte swizzle
 // (box_cols * 2 == 128).  Out-of-range elements load as zero.
+// Host-side fault injection for tests: LMHEAD_FAULT names a site --
+//   "tensor_map"  tensor-map encoding fails          (call returns ECUDA)
+//   "launch"      the first GEMM launch is refused    (call returns ECUDA)
+//   "stall"       the GEMM producer issues no loads   (device status ETIMEOUT)
+// Nothing here touches the GPU in a way that can fault or hang it.
+bool fault_at(const char* site) {
+  const char* e = std::getenv("LMHEAD_FAULT");
+  return e != nullptr && std::strcmp(e, site) == 0;
+}
+
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
               int box_rows, int box_cols) {
+  if (fault_at("tensor_map")) return false;
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -248,6 +259,7 @@ template <int MODE>
 cudaError_t run_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b_single,
                      const CUtensorMap& b_pair, const TcGemmParams& p, int64_t m_upper,
                      int64_t n, cudaStream_t s, int* workers = nullptr) {
+  if (fault_at("launch")) return cudaErrorLaunchFailure;
   const int split = MODE == kDh ? p.max_split : 1;
   if (pair) {
     const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, kBN) * split;
@@ -315,6 +327,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.H = H;
   p.group_n = 16;
   p.status = status;
+  p.stall = fault_at("stall") ? 1 : 0;
   p.targets_c = yc;
   p.want_entropy = want_entropy ? 1 : 0;
   p.part = part;
@@ -420,6 +433,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.V = V;
   p.H = H;
   p.status = status;
+  p.stall = fault_at("stall") ? 1 : 0;
   p.targets_c = yc;
   p.idx = idx;
   p.lse_c = lse_c;

@@ -170,24 +170,57 @@ __global__ void gather_vec_kernel(const int32_t* __restrict__ idx, const int32_t
 // Split-V merge of the per-tile (m, s, u, t) partials of one chunk:
 //   M = max m_i, S = sum s_i e^(m_i - M), U = sum e^(m_i - M)(u_i + s_i (m_i - M))
 //   lse = M + log S, logprob = t - lse, entropy = log S - U / S.
+// Four threads per row, each taking every fourth vocab tile with a running
+// max-shifted (M, S, U); the four are combined with shuffles in a fixed order.
+__device__ __forceinline__ void merge_pair(float& M, float& S, float& U, float m2, float s2,
+                                           float u2) {
+  if (m2 == -INFINITY) return;
+  if (M == -INFINITY) {
+    M = m2; S = s2; U = u2;
+    return;
+  }
+  const float N = fmaxf(M, m2);
+  const float a = expf(M - N), b = expf(m2 - N);
+  U = a * (U + S * (M - N)) + b * (u2 + s2 * (m2 - N));
+  S = a * S + b * s2;
+  M = N;
+}
+
 __global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const int32_t* d_nk,
                              int chunk_index, int chunk_rows, int want_entropy,
                              float* __restrict__ lp_c, float* __restrict__ ent_c,
                              float* __restrict__ lse_c, float4* __restrict__ raw_c) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
-  float M = -INFINITY;
-  for (int v = 0; v < num_vt; ++v) M = fmaxf(M, part[static_cast<int64_t>(v) * chunk_rows + r].x);
-  float S = 0.f, U = 0.f, T = -INFINITY;
-  for (int v = 0; v < num_vt; ++v) {
-    const float4 q = part[static_cast<int64_t>(v) * chunk_rows + r];
-    const float sc = expf(q.x - M);
-    S = fmaf(q.y, sc, S);
-    U = fmaf(sc, fmaf(q.y, q.x - M, q.z), U);
-    T = fmaxf(T, q.w);
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r = g >> 2;
+  const int sub = g & 3;
+  if ((blockIdx.x * blockDim.x) / 4 >= rows) return;  // whole block past the chunk
+  float M = -INFINITY, S = 0.f, U = 0.f, T = -INFINITY;
+  if (r < rows) {
+    for (int v = sub; v < num_vt; v += 4) {
+      const float4 q = part[static_cast<int64_t>(v) * chunk_rows + r];
+      merge_pair(M, S, U, q.x, q.y, q.z);
+      T = fmaxf(T, q.w);
+    }
   }
+#pragma unroll
+  for (int off = 1; off < 4; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
+    const float u2 = __shfl_xor_sync(0xffffffffu, U, off);
+    const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
+    // combine in a fixed order (lower sub first) so every thread agrees
+    if ((sub & off) == 0) {
+      merge_pair(M, S, U, m2, s2, u2);
+    } else {
+      float m1 = m2, s1 = s2, u1 = u2;
+      merge_pair(m1, s1, u1, M, S, U);
+      M = m1; S = s1; U = u1;
+    }
+    T = fmaxf(T, t2);
+  }
+  if (sub != 0 || r >= rows) return;
   if (raw_c != nullptr) {  // a vocabulary shard: keep the unnormalised reduction
     raw_c[chunk_start + r] = make_float4(M, S, U, T);
     return;
@@ -349,7 +382,8 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
 cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
                          float* lse_c, float4* raw_c, cudaStream_t s) {
-  merge_kernel<<<blocks_for(chunk_rows, 128), 128, 0, s>>>(part, num_vt, d_nk, chunk_index,
+  merge_kernel<<<blocks_for(static_cast<int64_t>(chunk_rows) * 4, 256), 256, 0, s>>>(
+      part, num_vt, d_nk, chunk_index,
                                                            chunk_rows, want_entropy, lp_c, ent_c,
                                                            lse_c, raw_c);
   return cudaGetLastError();

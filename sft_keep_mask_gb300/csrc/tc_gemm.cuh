@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && !p.stall; u += gridDim.x) {
         const int t = u % num_tiles;
         const int sidx = u / num_tiles;
         const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);

@@ -99,7 +99,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_a = make_l2_policy(p.hint_a);
       const uint64_t pol_b = make_l2_policy(p.hint_b);
       const bool ha = p.hint_a != 0, hb = p.hint_b != 0;
-      for (int u = pair; u < num_units; u += num_pairs) {
+      for (int u = pair; u < num_units && !p.stall; u += num_pairs) {
         const int t = u % num_tiles;
         const int sidx = u / num_tiles;
         const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
