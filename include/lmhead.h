@@ -288,6 +288,16 @@ lmhead_status lmhead_selective_log_softmax_bwd(const void* logits, int logits_dt
  */
 lmhead_status lmhead_get_status(const void* workspace, lmhead_stream_t stream);
 
+/*
+ * Device address (int32, 1 element) where lmhead_fwd / lmhead_bwd /
+ * lmhead_compact leave Nk, the number of kept rows of their last call on this
+ * workspace -- for logging the kept-token fraction Nk/N ([P1] Overview:
+ * perf/lm_head_token_fraction) without synchronising the host.  NULL for a
+ * NULL workspace.  The value is valid once that call has completed on its
+ * stream.
+ */
+const int32_t* lmhead_workspace_kept_rows(const void* workspace);
+
 /* Human-readable name of a status code (static string). */
 const char* lmhead_strerror(lmhead_status status);
 

@@ -61,5 +61,10 @@ class LMHeadScorer:
                      dhidden, dweight, accumulate, self.workspace, self.chunk_rows, stream)
         return dhidden, dweight
 
+    def kept_rows(self):
+        """Nk of the last call on this workspace, as a 1-element int32 CUDA
+        tensor (read it after the call has completed; no host sync here)."""
+        return L.lmhead_workspace_kept_rows(self.workspace)
+
     def status(self, stream=None) -> int:
         return L.lmhead_get_status(self.workspace, stream)

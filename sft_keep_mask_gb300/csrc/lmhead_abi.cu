@@ -11,6 +11,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/lmhead.h"
 #include "internal.h"
@@ -128,6 +129,13 @@ class Launch {
   int kind_;
   cudaStream_t s_;
   cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+// NVTX range over an entry point or a chunk (visible in Nsight timelines).
+class Range {
+ public:
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
 };
 
 // ------------------------------------------------------------ tensor maps
@@ -296,6 +304,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Range range("lmhead_fwd");
 
   int* status = at<int>(workspace, L.hdr);
   int32_t* d_nk = status + 1;
@@ -334,6 +343,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
 
   const int64_t max_chunks = cdiv(N, L.C);
   for (int64_t c = 0; c < max_chunks; ++c) {
+    Range chunk_range("chunk");
     {
       Launch l(kKindGatherRows, s);
       LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
@@ -385,6 +395,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   if (st != LMHEAD_OK) return st;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Range range("lmhead_bwd");
   if (N == 0) {
     if (!dw_accumulate)
       LM_TRY(cudaMemsetAsync(dweight, 0, static_cast<size_t>(V) * H * sizeof(float), s));
@@ -453,6 +464,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
 
   const int64_t max_chunks = cdiv(N, L.C);
   for (int64_t c = 0; c < max_chunks; ++c) {
+    Range chunk_range("chunk");
     p.chunk_index = static_cast<int>(c);
     {
       Launch l(kKindGatherRows, s);
@@ -618,6 +630,7 @@ lmhead_status lmhead_selective_log_softmax_fwd(const void* logits, int logits_dt
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Range range("lmhead_selective_log_softmax_fwd");
   Launch l(kKindSlsFwd, s);
   return cuda_status(launch_sls_fwd(logits, logits_dtype, ld, targets, keep, N, V,
                                     want_entropy ? 1 : 0, logprob, want_entropy ? entropy : nullptr,
@@ -640,9 +653,15 @@ lmhead_status lmhead_selective_log_softmax_bwd(const void* logits, int logits_dt
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Range range("lmhead_selective_log_softmax_bwd");
   Launch l(kKindSlsBwd, s);
   return cuda_status(launch_sls_bwd(logits, logits_dtype, ld, targets, keep, N, V, lse, entropy,
                                     grad_logprob, grad_entropy, dlogits, ld_out, d_status, s));
+}
+
+const int32_t* lmhead_workspace_kept_rows(const void* workspace) {
+  if (workspace == nullptr) return nullptr;
+  return reinterpret_cast<const int32_t*>(static_cast<const char*>(workspace) + sizeof(int32_t));
 }
 
 lmhead_status lmhead_get_status(const void* workspace, lmhead_stream_t stream) {

@@ -170,8 +170,12 @@ __global__ void gather_vec_kernel(const int32_t* __restrict__ idx, const int32_t
 // Split-V merge of the per-tile (m, s, u, t) partials of one chunk:
 //   M = max m_i, S = sum s_i e^(m_i - M), U = sum e^(m_i - M)(u_i + s_i (m_i - M))
 //   lse = M + log S, logprob = t - lse, entropy = log S - U / S.
-// Four threads per row, each taking every fourth vocab tile with a running
-// max-shifted (M, S, U); the four are combined with shuffles in a fixed order.
+// kMergeLanes threads per row, each taking every kMergeLanes-th vocab tile with
+// a running max-shifted (M, S, U); the lanes of a row are combined with
+// shuffles.  Two rows per warp: each load instruction of a warp touches 16
+// vocab tiles x 2 consecutive rows = 16 full 32-byte sectors.
+constexpr int kMergeLanes = 16;
+
 __device__ __forceinline__ void merge_pair(float& M, float& S, float& U, float m2, float s2,
                                            float u2) {
   if (m2 == -INFINITY) return;
@@ -192,25 +196,37 @@ __global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const 
                              float* __restrict__ lse_c, float4* __restrict__ raw_c) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
+  if (static_cast<int>((blockIdx.x * blockDim.x) / kMergeLanes) >= rows) return;  // whole block
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
-  const int r = g >> 2;
-  const int sub = g & 3;
-  if ((blockIdx.x * blockDim.x) / 4 >= rows) return;  // whole block past the chunk
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & (kMergeLanes - 1);
+  const int r = (g >> 5) * (32 / kMergeLanes) + (lane / kMergeLanes);
   float M = -INFINITY, S = 0.f, U = 0.f, T = -INFINITY;
   if (r < rows) {
-    for (int v = sub; v < num_vt; v += 4) {
+    int v = sub;
+    for (; v + 3 * kMergeLanes < num_vt; v += 4 * kMergeLanes) {
+      float4 q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) q[k] = part[static_cast<int64_t>(v + k * kMergeLanes) * chunk_rows + r];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        merge_pair(M, S, U, q[k].x, q[k].y, q[k].z);
+        T = fmaxf(T, q[k].w);
+      }
+    }
+    for (; v < num_vt; v += kMergeLanes) {
       const float4 q = part[static_cast<int64_t>(v) * chunk_rows + r];
       merge_pair(M, S, U, q.x, q.y, q.z);
       T = fmaxf(T, q.w);
     }
   }
 #pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
+  for (int off = 1; off < kMergeLanes; off <<= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
     const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
     const float u2 = __shfl_xor_sync(0xffffffffu, U, off);
     const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
-    // combine in a fixed order (lower sub first) so every thread agrees
+    // the lower lane's value first, so both lanes of a pair hold the same sum
     if ((sub & off) == 0) {
       merge_pair(M, S, U, m2, s2, u2);
     } else {
@@ -382,7 +398,7 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
 cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
                          float* lse_c, float4* raw_c, cudaStream_t s) {
-  merge_kernel<<<blocks_for(static_cast<int64_t>(chunk_rows) * 4, 256), 256, 0, s>>>(
+  merge_kernel<<<blocks_for(static_cast<int64_t>(chunk_rows) * kMergeLanes, 256), 256, 0, s>>>(
       part, num_vt, d_nk, chunk_index,
                                                            chunk_rows, want_entropy, lp_c, ent_c,
                                                            lse_c, raw_c);

@@ -55,6 +55,7 @@ _SIGS = {
     "lmhead_selective_log_softmax_bwd": (_I32, [_VP, _I32, _I64, _VP, _VP, _I64, _I32, _VP, _VP,
                                                 _VP, _VP, _VP, _I64, _VP, _VP]),
     "lmhead_get_status": (_I32, [_VP, _VP]),
+    "lmhead_workspace_kept_rows": (_VP, [_VP]),
     "lmhead_strerror": (ctypes.c_char_p, [_I32]),
     "lmhead_profile_enable": (None, [_I32]),
     "lmhead_profile_kinds": (_I32, []),
@@ -302,6 +303,13 @@ def lmhead_selective_log_softmax_bwd(logits, targets, keep, lse, entropy, grad_l
 def lmhead_get_status(workspace, stream=None) -> int:
     """Device status of the last call on this workspace (synchronises)."""
     return int(lib().lmhead_get_status(_p(workspace), _s(stream)))
+
+
+def lmhead_workspace_kept_rows(workspace):
+    """A 1-element int32 CUDA tensor viewing Nk in the workspace (no copy)."""
+    addr = lib().lmhead_workspace_kept_rows(_p(workspace))
+    off = addr - workspace.data_ptr()
+    return workspace[off:off + 4].view(torch.int32)
 
 
 def lmhead_profile_enable(on: bool = True):
