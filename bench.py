@@ -367,31 +367,18 @@ def run_ours(args):
         pin = lambda t: t.cpu().pin_memory() if t is not None else None  # noqa: E731
         host = [pin(inp["hidden"]), pin(inp["targets"]), pin(loss_mask), pin(offsets),
                 pin(inp["grad_logprob"]), pin(g_ent)]
-        dbuf = [torch.empty_like(t, device=dev) if t is not None else None for t in host]
-        out_lp = torch.empty(N, dtype=torch.float32).pin_memory()
-        out_ent = torch.empty(N, dtype=torch.float32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
         d2h = 2 * N * 4
         if args.keep_off:
             host[2] = host[3] = None
-            dbuf[2] = dbuf[3] = None
             h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
 
-        def e2e_step():
-            for d, hst in zip(dbuf, host):
-                if d is not None:
-                    d.copy_(hst, non_blocking=True)
-            step(*dbuf)
-            out_lp.copy_(lp, non_blocking=True)
-            out_ent.copy_(ent, non_blocking=True)
-            stream.synchronize()
-
-        for _ in range(2):
-            e2e_step()
+        from sft_keep_mask_gb300.api import StepPipeline
+        pipe = StepPipeline(step, lambda: (lp, ent), host, device=dev)
+        pipe.run([host] * 2)
         barrier()
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
+        pipe.run([host] * args.steps)
         barrier()
         el = time.perf_counter() - t0
         el, _ = reduce_over_ranks(el, 0, world, dev)

@@ -68,3 +68,59 @@ class LMHeadScorer:
 
     def status(self, stream=None) -> int:
         return L.lmhead_get_status(self.workspace, stream)
+
+
+class StepPipeline:
+    """Runs steps whose inputs live in pinned host memory, overlapping the
+    host-to-device copy of step i+1's inputs with the computation of step i.
+
+    step_fn(*device_inputs) enqueues one step on the current stream (e.g. the
+    keep mask, lmhead_fwd and lmhead_bwd calls); result_fn() returns the
+    device tensors to read back after every step (e.g. logprob and entropy).
+    Two sets of device input buffers alternate; a side stream does the
+    copies, ordered against the computation with events.
+    """
+
+    def __init__(self, step_fn, result_fn, host_inputs, device="cuda"):
+        self.device = torch.device(device)
+        self.step_fn = step_fn
+        self.result_fn = result_fn
+        self.copy_stream = torch.cuda.Stream(self.device)
+        self.bufs = [[None if t is None else torch.empty_like(t, device=self.device)
+                      for t in host_inputs] for _ in range(2)]
+        self.ready = [torch.cuda.Event() for _ in range(2)]
+        self.free = [torch.cuda.Event() for _ in range(2)]
+        for e in self.free:
+            e.record(torch.cuda.current_stream(self.device))
+        self.host_results = None
+
+    def _prefetch(self, slot, host_inputs):
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.free[slot])
+            for d, h in zip(self.bufs[slot], host_inputs):
+                if d is not None:
+                    d.copy_(h, non_blocking=True)
+            self.ready[slot].record(self.copy_stream)
+
+    def run(self, batches):
+        """Runs one step per batch (a list of pinned host tensors each);
+        returns the host copies of the last step's results."""
+        compute = torch.cuda.current_stream(self.device)
+        if not batches:
+            return self.host_results
+        self._prefetch(0, batches[0])
+        for i in range(len(batches)):
+            slot = i % 2
+            if i + 1 < len(batches):
+                self._prefetch(1 - slot, batches[i + 1])
+            compute.wait_event(self.ready[slot])
+            self.step_fn(*self.bufs[slot])
+            self.free[slot].record(compute)
+            res = self.result_fn()
+            if self.host_results is None:
+                self.host_results = [torch.empty(r.shape, dtype=r.dtype).pin_memory()
+                                     for r in res]
+            for h, r in zip(self.host_results, res):
+                h.copy_(r, non_blocking=True)
+            compute.synchronize()  # the step's result is read on the host
+        return self.host_results

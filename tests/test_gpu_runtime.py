@@ -63,3 +63,40 @@ def test_kept_rows_on_the_device():
     sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
     torch.cuda.synchronize()
     assert int(sc.kept_rows().item()) == int(inp["keep"].sum().item())
+
+
+def test_step_pipeline_overlapped_copies_give_the_same_results():
+    # three different batches in pinned host memory; the pipeline copies batch
+    # i+1 while batch i computes and must return what direct calls return
+    from sft_keep_mask_gb300.api import StepPipeline
+    w = synth.workload("tiny", seed=132, N=800, H=128, V=2000)
+    batches, direct = [], []
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
+    weight = synth.make_inputs(w, device=DEV)["weight"]
+    for k in range(3):
+        inp = synth.make_inputs(synth.workload("tiny", seed=133 + k, N=800, H=128, V=2000),
+                                device=DEV)
+        lp, ent, _ = sc.forward(inp["hidden"], weight, inp["targets"], inp["keep"])
+        torch.cuda.synchronize()
+        direct.append((lp.cpu(), ent.cpu()))
+        batches.append([inp["hidden"].cpu().pin_memory(), inp["targets"].cpu().pin_memory(),
+                        inp["keep"].cpu().pin_memory()])
+    lp = torch.empty(w.N, device=DEV)
+    ent = torch.empty(w.N, device=DEV)
+    lse = torch.empty(w.N, device=DEV)
+    seen = []
+
+    def step(hidden, targets, keep):
+        sc.forward(hidden, weight, targets, keep, out=(lp, ent, lse))
+
+    def result():
+        return lp, ent
+
+    pipe = StepPipeline(step, result, batches[0], device=DEV)
+    for b, want in zip(batches, direct):
+        out = pipe.run([b])
+        seen.append((out[0].clone(), out[1].clone()))
+    out = pipe.run(batches)  # all three back to back: the last one is returned
+    assert torch.equal(out[0], direct[-1][0]) and torch.equal(out[1], direct[-1][1])
+    for (a, b), (c, d) in zip(seen, direct):
+        assert torch.equal(a, c) and torch.equal(b, d)
