@@ -190,6 +190,29 @@ lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64_t* targets
                                      int32_t* d_status, lmhead_stream_t stream);
 
 /*
+ * Block-sparse form (tile skipping in place; [P2] "How it works": block-sparse
+ * forward and backward skip inactive tiles instead of compacting).  Same
+ * arguments, results and workspace as lmhead_fwd / lmhead_bwd; instead of
+ * compacting kept rows, the 256-row tiles of the batch that hold at least one
+ * kept row are scored where they lie (hidden is read in place, no gather or
+ * scatter); rows of those tiles that are not kept get the same zeros and add
+ * nothing to dW.  It does the work of every row of an active tile, so it pays
+ * off only when kept rows come in tile-aligned spans.
+ */
+lmhead_status lmhead_fwd_blocksparse(const void* hidden, const void* weight,
+                                     const int64_t* targets, const uint8_t* keep, int64_t N,
+                                     int H, int V, int want_entropy, float* logprob,
+                                     float* entropy, float* lse, int chunk_rows, void* workspace,
+                                     size_t ws_bytes, lmhead_stream_t stream);
+lmhead_status lmhead_bwd_blocksparse(const void* hidden, const void* weight,
+                                     const int64_t* targets, const uint8_t* keep, int64_t N,
+                                     int H, int V, const float* lse, const float* entropy,
+                                     const float* grad_logprob, const float* grad_entropy,
+                                     void* dhidden, float* dweight, int dw_accumulate,
+                                     int chunk_rows, void* workspace, size_t ws_bytes,
+                                     lmhead_stream_t stream);
+
+/*
  * Vocabulary-parallel form ([P2] gemini-code-assist review: with the LM head
  * split over the vocabulary, each rank reduces its own logits and one
  * exchange after the loop completes the log-softmax and the entropy; greptile

@@ -11,10 +11,12 @@ from .lmhead import (  # noqa: F401
     LmheadError,
     lmhead_build_keep_mask,
     lmhead_bwd,
+    lmhead_bwd_blocksparse,
     lmhead_bwd_shard,
     lmhead_compact,
     lmhead_expand,
     lmhead_fwd,
+    lmhead_fwd_blocksparse,
     lmhead_fwd_shard,
     lmhead_get_status,
     lmhead_launch_count,

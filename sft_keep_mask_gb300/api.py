@@ -14,8 +14,12 @@ from . import lmhead as L
 class LMHeadScorer:
     """Fused LM-head scoring for fixed (N, H, V, chunk_rows)."""
 
-    def __init__(self, N: int, H: int, V: int, chunk_rows: int = 0, device="cuda"):
+    def __init__(self, N: int, H: int, V: int, chunk_rows: int = 0, device="cuda",
+                 blocksparse: bool = False):
+        """blocksparse: score the active 256-row tiles in place instead of
+        compacting the kept rows (lmhead_fwd_blocksparse / _bwd_blocksparse)."""
         self.N, self.H, self.V = N, H, V
+        self.blocksparse = blocksparse
         self.chunk_rows = chunk_rows
         self.device = torch.device(device)
         nbytes = L.lmhead_workspace_size(N, H, V, True, chunk_rows)
@@ -47,8 +51,9 @@ class LMHeadScorer:
                    if want_entropy else None,
                    torch.empty(self.N, dtype=torch.float32, device=self.device))
         lp, ent, lse = out
-        L.lmhead_fwd(hidden, weight, targets, keep, want_entropy, lp, ent, lse, self.workspace,
-                     self.chunk_rows, stream)
+        fwd = L.lmhead_fwd_blocksparse if self.blocksparse else L.lmhead_fwd
+        fwd(hidden, weight, targets, keep, want_entropy, lp, ent, lse, self.workspace,
+            self.chunk_rows, stream)
         return lp, ent, lse
 
     def backward(self, hidden, weight, targets, keep, lse, entropy, grad_logprob,
@@ -57,8 +62,9 @@ class LMHeadScorer:
             dhidden = torch.empty_like(hidden)
         if dweight is None:
             dweight = torch.empty(self.V, self.H, dtype=torch.float32, device=self.device)
-        L.lmhead_bwd(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_entropy,
-                     dhidden, dweight, accumulate, self.workspace, self.chunk_rows, stream)
+        bwd = L.lmhead_bwd_blocksparse if self.blocksparse else L.lmhead_bwd
+        bwd(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_entropy, dhidden,
+            dweight, accumulate, self.workspace, self.chunk_rows, stream)
         return dhidden, dweight
 
     def kept_rows(self):
@@ -71,14 +77,16 @@ class LMHeadScorer:
 
 
 class StepPipeline:
-    """Runs steps whose inputs live in pinned host memory, overlapping the
-    host-to-device copy of step i+1's inputs with the computation of step i.
+    """Runs steps whose inputs live in pinned host memory, keeping the GPU busy
+    across steps: the host-to-device copy of step i+1's inputs overlaps the
+    computation of step i, and the host reads step i's results while step
+    i+1 is already queued.
 
     step_fn(*device_inputs) enqueues one step on the current stream (e.g. the
     keep mask, lmhead_fwd and lmhead_bwd calls); result_fn() returns the
     device tensors to read back after every step (e.g. logprob and entropy).
-    Two sets of device input buffers alternate; a side stream does the
-    copies, ordered against the computation with events.
+    Two sets of device input buffers and two sets of pinned result buffers
+    alternate; a side stream does the copies, ordered with events.
     """
 
     def __init__(self, step_fn, result_fn, host_inputs, device="cuda"):
@@ -90,6 +98,7 @@ class StepPipeline:
                       for t in host_inputs] for _ in range(2)]
         self.ready = [torch.cuda.Event() for _ in range(2)]
         self.free = [torch.cuda.Event() for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
         for e in self.free:
             e.record(torch.cuda.current_stream(self.device))
         self.host_results = None
@@ -103,11 +112,12 @@ class StepPipeline:
             self.ready[slot].record(self.copy_stream)
 
     def run(self, batches):
-        """Runs one step per batch (a list of pinned host tensors each);
-        returns the host copies of the last step's results."""
+        """Runs one step per batch (a list of pinned host tensors each), reading
+        every step's results back; returns the host copies of the last step's."""
         compute = torch.cuda.current_stream(self.device)
         if not batches:
-            return self.host_results
+            return None
+        pending = None
         self._prefetch(0, batches[0])
         for i in range(len(batches)):
             slot = i % 2
@@ -118,9 +128,13 @@ class StepPipeline:
             self.free[slot].record(compute)
             res = self.result_fn()
             if self.host_results is None:
-                self.host_results = [torch.empty(r.shape, dtype=r.dtype).pin_memory()
-                                     for r in res]
-            for h, r in zip(self.host_results, res):
+                self.host_results = [[torch.empty(r.shape, dtype=r.dtype).pin_memory()
+                                      for r in res] for _ in range(2)]
+            for h, r in zip(self.host_results[slot], res):
                 h.copy_(r, non_blocking=True)
-            compute.synchronize()  # the step's result is read on the host
-        return self.host_results
+            self.done[slot].record(compute)
+            if pending is not None:
+                pending.synchronize()  # step i-1's results are on the host
+            pending = self.done[slot]
+        pending.synchronize()
+        return self.host_results[(len(batches) - 1) % 2]

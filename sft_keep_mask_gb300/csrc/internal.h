@@ -55,6 +55,10 @@ struct TcGemmParams {
   int split_fill_pct;       // kDh: split only below this fill of the worker slots
   int stall;                // fault injection: the producer issues no loads, so
                             //   the pipeline waits run out (device ETIMEOUT)
+  // Block-sparse mode (tile skipping in place): the "compact rows" are the
+  // rows of the active 256-row tiles of the batch, read from hidden directly.
+  const int32_t* tile_list; // active tiles (row / 256), or nullptr (compaction)
+  const uint8_t* lvalid;    // per compact row: 1 if it is a kept row
 };
 
 template <int MODE>
@@ -116,6 +120,13 @@ __host__ __device__ __forceinline__ int dh_split_count(int tiles, int workers, i
   return best;
 }
 
+// Block-sparse mode: row of the hidden states behind compact row (cstart + lrow),
+// where the compact rows are the rows of the active 256-row tiles in order.
+__device__ __forceinline__ int sparse_row(const int32_t* tile_list, int cstart, int lrow) {
+  const int l = cstart + lrow;
+  return tile_list[l >> 8] * 256 + (l & 255);
+}
+
 // Rows counted by one block of the compaction scan (rowops.cu).
 constexpr int kCompactRowsPerBlock = 4096;
 
@@ -127,6 +138,16 @@ cudaError_t launch_build_keep(const float* c0, const float* c1, const float* c2,
 cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t N,
                            int64_t V_valid, int64_t t_offset, int32_t* idx, int32_t* targets_c,
                            int32_t* d_nk, int32_t* counts, int* status, cudaStream_t s);
+// Block-sparse mode: active 256-row tiles (any kept row), compacted to
+// tile_list[0..Na) with Na at d_na; then the per-compact-row arrays for the
+// Na * 256 rows of those tiles: idx (row of the batch, clamped to N-1),
+// targets_c (checked against [0, V_valid), minus t_offset), lvalid (kept
+// row), and d_nk = Na * 256.
+cudaError_t launch_tile_scan(const uint8_t* keep, const int64_t* targets, int64_t N,
+                             int64_t V_valid, int64_t t_offset, uint8_t* tile_flags,
+                             int32_t* tile_list, int32_t* d_na, int32_t* counts, int32_t* idx,
+                             int32_t* targets_c, uint8_t* lvalid, int32_t* d_nk, int* status,
+                             cudaStream_t s);
 cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
                                const int32_t* d_nk, int chunk_index, int chunk_rows, int H,
                                __nv_bfloat16* hc, cudaStream_t s);
@@ -140,7 +161,7 @@ cudaError_t launch_expand4(const uint8_t* keep, const int32_t* idx, const int32_
                            const float4* src, float4* dst, cudaStream_t s);
 cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,
                            int64_t N, const float* a_c, const float* b_c, const float* c_c,
-                           float* a, float* b, float* c, cudaStream_t s);
+                           float* a, float* b, float* c, const uint8_t* lvalid, cudaStream_t s);
 cudaError_t launch_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,
                           float* dst, cudaStream_t s);
 cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N,
@@ -151,7 +172,7 @@ cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N
 cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
                              int chunk_rows, int H, int tile_m, int workers, int num_kb,
                              int max_split, int fill_pct, const int32_t* idx,
-                             __nv_bfloat16* dhidden, cudaStream_t s);
+                             const uint8_t* lvalid, __nv_bfloat16* dhidden, cudaStream_t s);
 cudaError_t launch_zero_skipped_rows(const uint8_t* keep, int64_t N, int H,
                                      __nv_bfloat16* dhidden, cudaStream_t s);
 

@@ -34,7 +34,7 @@ struct Layout {
   int64_t num_vt = 0;   // 256-wide vocab tiles
   int64_t dz_ld = 0;    // row stride of the dZ chunk buffer (elements)
   size_t hdr = 0, counts = 0, idx = 0, yc = 0, v0 = 0, v1 = 0, v2 = 0, v3 = 0, p4 = 0, hc = 0,
-         part = 0, dz = 0, dhp = 0, total = 0;
+         part = 0, dz = 0, dhp = 0, tflags = 0, tlist = 0, lvalid = 0, total = 0;
 };
 
 Layout make_layout(int64_t N, int H, int V, int chunk_rows) {
@@ -52,17 +52,24 @@ Layout make_layout(int64_t N, int H, int V, int chunk_rows) {
   };
   L.hdr = take(256);
   L.counts = take(static_cast<size_t>(cdiv(N, 4096) + 1) * 4);
-  L.idx = take(static_cast<size_t>(N) * 4);
-  L.yc = take(static_cast<size_t>(N) * 4);
-  L.v0 = take(static_cast<size_t>(N) * 4);
-  L.v1 = take(static_cast<size_t>(N) * 4);
-  L.v2 = take(static_cast<size_t>(N) * 4);
-  L.v3 = take(static_cast<size_t>(N) * 4);
-  L.p4 = take(static_cast<size_t>(N) * 16);
+  // per-compact-row arrays hold up to N rounded up to 256 rows (the rows of
+  // the active tiles in block-sparse mode)
+  const size_t NP = static_cast<size_t>(round_up(N, 256));
+  const size_t T = NP / 256;
+  L.idx = take(NP * 4);
+  L.yc = take(NP * 4);
+  L.v0 = take(NP * 4);
+  L.v1 = take(NP * 4);
+  L.v2 = take(NP * 4);
+  L.v3 = take(NP * 4);
+  L.p4 = take(NP * 16);
   L.hc = take(static_cast<size_t>(L.C) * H * 2);
   L.part = take(static_cast<size_t>(L.num_vt) * L.C * 16);
   L.dz = take(static_cast<size_t>(L.C) * L.dz_ld * 2);
   L.dhp = take(static_cast<size_t>(kDhMaxSplit) * L.C * H * 4);
+  L.tflags = take(T + 1);
+  L.tlist = take((T + 1) * 4);
+  L.lvalid = take(NP);
   L.total = off;
   return L;
 }
@@ -289,7 +296,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
                        const uint8_t* keep, int64_t N, int H, int V, int want_entropy,
                        float* logprob, float* entropy, float* lse, float4* partial,
                        int64_t t_offset, int64_t V_valid, int chunk_rows, void* workspace,
-                       size_t ws_bytes, lmhead_stream_t stream) {
+                       size_t ws_bytes, lmhead_stream_t stream, bool blocksparse = false) {
   lmhead_status st = check_sizes(N, H, V);
   if (st != LMHEAD_OK) return st;
   if (hidden == nullptr || weight == nullptr || targets == nullptr)
@@ -318,13 +325,24 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   float4* part = at<float4>(workspace, L.part);
 
   LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
-  st = run_compact(keep, targets, N, V_valid, t_offset, idx, yc, d_nk,
-                   at<int32_t>(workspace, L.counts), status, s);
+  uint8_t* lvalid = blocksparse ? at<uint8_t>(workspace, L.lvalid) : nullptr;
+  int32_t* tile_list = at<int32_t>(workspace, L.tlist);
+  if (blocksparse) {
+    Launch l(kKindCompact, s, 4);
+    LM_TRY(launch_tile_scan(keep, targets, N, V_valid, t_offset, at<uint8_t>(workspace, L.tflags),
+                            tile_list, status + 2, at<int32_t>(workspace, L.counts), idx, yc,
+                            lvalid, d_nk, status, s));
+    st = LMHEAD_OK;
+  } else {
+    st = run_compact(keep, targets, N, V_valid, t_offset, idx, yc, d_nk,
+                     at<int32_t>(workspace, L.counts), status, s);
+  }
   if (st != LMHEAD_OK) return st;
 
   const bool pair = use_pair();
   CUtensorMap ma, mb, mb2;
-  if (!make_map(&ma, hc, L.C, H, H, kBM, 64) ||
+  if (!(blocksparse ? make_map(&ma, hidden, N, H, H, kBM, 64)
+                    : make_map(&ma, hc, L.C, H, H, kBM, 64)) ||
       !make_map(&mb, weight, V, H, H, kBN, 64) ||
       !make_map(&mb2, weight, V, H, H, 128, 64))
     return LMHEAD_ECUDA;
@@ -337,6 +355,8 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.group_n = 16;
   p.status = status;
   p.stall = fault_at("stall") ? 1 : 0;
+  p.tile_list = blocksparse ? tile_list : nullptr;
+  p.lvalid = lvalid;
   p.targets_c = yc;
   p.want_entropy = want_entropy ? 1 : 0;
   p.part = part;
@@ -344,7 +364,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   const int64_t max_chunks = cdiv(N, L.C);
   for (int64_t c = 0; c < max_chunks; ++c) {
     Range chunk_range("chunk");
-    {
+    if (!blocksparse) {
       Launch l(kKindGatherRows, s);
       LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
                                 static_cast<int>(c), static_cast<int>(L.C), H, hc, s));
@@ -366,7 +386,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
       LM_TRY(launch_expand4(keep, idx, d_nk, N, raw_c, partial, s));
     } else {
       LM_TRY(launch_expand3(keep, idx, d_nk, N, lp_c, want_entropy ? ent_c : nullptr, lse_c,
-                            logprob, want_entropy ? entropy : nullptr, lse, s));
+                            logprob, want_entropy ? entropy : nullptr, lse, lvalid, s));
     }
   }
   return LMHEAD_OK;
@@ -381,7 +401,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
                        int64_t V_valid, const float* lse, const float* entropy,
                        const float* grad_logprob, const float* grad_entropy, void* dhidden,
                        float* dweight, int dw_accumulate, int chunk_rows, void* workspace,
-                       size_t ws_bytes, lmhead_stream_t stream) {
+                       size_t ws_bytes, lmhead_stream_t stream, bool blocksparse = false) {
   lmhead_status st = check_sizes(N, H, V);
   if (st != LMHEAD_OK) return st;
   if (hidden == nullptr || weight == nullptr || targets == nullptr || lse == nullptr ||
@@ -414,8 +434,18 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   __nv_bfloat16* dz = at<__nv_bfloat16>(workspace, L.dz);
 
   LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
-  st = run_compact(keep, targets, N, V_valid, t_offset, idx, yc, d_nk,
-                   at<int32_t>(workspace, L.counts), status, s);
+  uint8_t* lvalid = blocksparse ? at<uint8_t>(workspace, L.lvalid) : nullptr;
+  int32_t* tile_list = at<int32_t>(workspace, L.tlist);
+  if (blocksparse) {
+    Launch l(kKindCompact, s, 4);
+    LM_TRY(launch_tile_scan(keep, targets, N, V_valid, t_offset, at<uint8_t>(workspace, L.tflags),
+                            tile_list, status + 2, at<int32_t>(workspace, L.counts), idx, yc,
+                            lvalid, d_nk, status, s));
+    st = LMHEAD_OK;
+  } else {
+    st = run_compact(keep, targets, N, V_valid, t_offset, idx, yc, d_nk,
+                     at<int32_t>(workspace, L.counts), status, s);
+  }
   if (st != LMHEAD_OK) return st;
   {
     Launch l(kKindGatherVec, s);
@@ -429,13 +459,15 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
 
   const bool pair = use_pair();
   CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn;
-  if (!make_map(&m_hc_k, hc, L.C, H, H, kBM, 64) ||        // A of kDz (K-major)
+  const void* rows_src = blocksparse ? hidden : static_cast<const void*>(hc);
+  const int64_t rows_n = blocksparse ? N : L.C;
+  if (!make_map(&m_hc_k, rows_src, rows_n, H, H, kBM, 64) ||  // A of kDz (K-major)
       !make_map(&m_w_k, weight, V, H, H, kBN, 64) ||       // B of kDz (K-major)
       !make_map(&m_w_k2, weight, V, H, H, 128, 64) ||      // B of kDz, CTA pairs
       !make_map(&m_dz_k, dz, L.C, V, L.dz_ld, kBM, 64) ||  // A of kDh (K-major)
       !make_map(&m_w_mn, weight, V, H, H, 64, 64) ||       // B of kDh (MN-major boxes)
       !make_map(&m_dz_mn, dz, L.C, V, L.dz_ld, 64, 64) ||  // A of kDw (MN-major boxes)
-      !make_map(&m_hc_mn, hc, L.C, H, H, 64, 64))          // B of kDw (MN-major boxes)
+      !make_map(&m_hc_mn, rows_src, rows_n, H, H, 64, 64))  // B of kDw (MN-major boxes)
     return LMHEAD_ECUDA;
 
   TcGemmParams p{};
@@ -447,6 +479,8 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.stall = fault_at("stall") ? 1 : 0;
   p.targets_c = yc;
   p.idx = idx;
+  p.tile_list = blocksparse ? tile_list : nullptr;
+  p.lvalid = lvalid;
   p.lse_c = lse_c;
   p.ent_c = ent_c;
   p.glp_c = glp_c;
@@ -466,7 +500,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   for (int64_t c = 0; c < max_chunks; ++c) {
     Range chunk_range("chunk");
     p.chunk_index = static_cast<int>(c);
-    {
+    if (!blocksparse) {
       Launch l(kKindGatherRows, s);
       LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
                                 static_cast<int>(c), static_cast<int>(L.C), H, hc, s));
@@ -485,7 +519,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       Launch l(kKindDhReduce, s);
       LM_TRY(launch_dh_reduce(p.dh_part, d_nk, static_cast<int>(c), static_cast<int>(L.C), H,
                               pair ? 256 : kBM, dh_workers, static_cast<int>(cdiv(V, kBK)),
-                              p.max_split, p.split_fill_pct, idx,
+                              p.max_split, p.split_fill_pct, idx, lvalid,
                               static_cast<__nv_bfloat16*>(dhidden), s));
     }
     {
@@ -563,6 +597,27 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
   return bwd_impl(hidden, weight, targets, keep, N, H, V, 0, V, lse, entropy, grad_logprob,
                   grad_entropy, dhidden, dweight, dw_accumulate, chunk_rows, workspace, ws_bytes,
                   stream);
+}
+
+lmhead_status lmhead_fwd_blocksparse(const void* hidden, const void* weight,
+                                     const int64_t* targets, const uint8_t* keep, int64_t N,
+                                     int H, int V, int want_entropy, float* logprob,
+                                     float* entropy, float* lse, int chunk_rows, void* workspace,
+                                     size_t ws_bytes, lmhead_stream_t stream) {
+  return fwd_impl(hidden, weight, targets, keep, N, H, V, want_entropy, logprob, entropy, lse,
+                  nullptr, 0, V, chunk_rows, workspace, ws_bytes, stream, true);
+}
+
+lmhead_status lmhead_bwd_blocksparse(const void* hidden, const void* weight,
+                                     const int64_t* targets, const uint8_t* keep, int64_t N,
+                                     int H, int V, const float* lse, const float* entropy,
+                                     const float* grad_logprob, const float* grad_entropy,
+                                     void* dhidden, float* dweight, int dw_accumulate,
+                                     int chunk_rows, void* workspace, size_t ws_bytes,
+                                     lmhead_stream_t stream) {
+  return bwd_impl(hidden, weight, targets, keep, N, H, V, 0, V, lse, entropy, grad_logprob,
+                  grad_entropy, dhidden, dweight, dw_accumulate, chunk_rows, workspace, ws_bytes,
+                  stream, true);
 }
 
 lmhead_status lmhead_fwd_shard(const void* hidden, const void* weight_shard,

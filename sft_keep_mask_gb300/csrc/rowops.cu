@@ -114,13 +114,15 @@ __global__ void scatter_kernel(const uint8_t* __restrict__ keep,
   for (int j = 0; j < kScanPerThread; ++j) {
     if (bits & (1u << j)) {
       const int64_t r = base + j;
-      int64_t y = targets[r];
-      if (y < 0 || y >= V_valid) {
-        atomicCAS(status, 0, kStatusTarget);
-        y = 0;
-      }
       idx[pos] = static_cast<int32_t>(r);
-      targets_c[pos] = static_cast<int32_t>(y - t_offset);
+      if (targets != nullptr) {  // (null when compacting tiles rather than rows)
+        int64_t y = targets[r];
+        if (y < 0 || y >= V_valid) {
+          atomicCAS(status, 0, kStatusTarget);
+          y = 0;
+        }
+        targets_c[pos] = static_cast<int32_t>(y - t_offset);
+      }
       ++pos;
     }
   }
@@ -129,6 +131,45 @@ __global__ void scatter_kernel(const uint8_t* __restrict__ keep,
     for (int j = 0; j < kScanThreads / 32; ++j) tot += warp_tot[j];
     *d_nk = offset + tot;
   }
+}
+
+// ------------------------------------------------------ block-sparse tiles
+// tile_flags[t] = 1 iff some row of rows [256 t, 256 t + 256) is kept.
+__global__ void tile_flags_kernel(const uint8_t* __restrict__ keep, int64_t N,
+                                  uint8_t* __restrict__ flags) {
+  const int64_t t = blockIdx.x;
+  const int64_t r = t * 256 + threadIdx.x;
+  const int k = (r < N && (keep == nullptr || keep[r] != 0)) ? 1 : 0;
+  const int any = __syncthreads_or(k);
+  if (threadIdx.x == 0) flags[t] = any ? 1 : 0;
+}
+
+// Per compact row l of the active tiles: the batch row behind it, its target
+// and whether it is kept.  Rows past N (last tile) are not kept and point at
+// row N-1 so that nothing reads out of bounds.
+__global__ void tile_rows_kernel(const uint8_t* __restrict__ keep,
+                                 const int64_t* __restrict__ targets, int64_t N, int64_t V_valid,
+                                 int64_t t_offset, const int32_t* __restrict__ tile_list,
+                                 const int32_t* d_na, int32_t* __restrict__ idx,
+                                 int32_t* __restrict__ targets_c, uint8_t* __restrict__ lvalid,
+                                 int32_t* d_nk, int* status) {
+  const int na = *d_na;
+  const int64_t l = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (l == 0) *d_nk = na * 256;
+  if (l >= static_cast<int64_t>(na) * 256) return;
+  const int64_t r = static_cast<int64_t>(tile_list[l >> 8]) * 256 + (l & 255);
+  const bool kept = r < N && (keep == nullptr || keep[r] != 0);
+  int64_t y = 0;
+  if (kept) {
+    y = targets[r];
+    if (y < 0 || y >= V_valid) {
+      atomicCAS(status, 0, kStatusTarget);
+      y = 0;
+    }
+  }
+  idx[l] = static_cast<int32_t>(r < N ? r : N - 1);
+  targets_c[l] = static_cast<int32_t>(y - t_offset);
+  lvalid[l] = kept ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ gathers
@@ -289,19 +330,19 @@ __global__ void expand4_kernel(const uint8_t* __restrict__ keep, const int32_t* 
 }
 
 // ------------------------------------------------------------------- expand
-// Disjoint writes: skipped rows get +0.0, kept row idx[k] gets value k.
+// Disjoint writes: skipped rows get +0.0, kept row idx[k] gets value k (in
+// block-sparse mode only the compact rows with lvalid set are kept rows).
 __global__ void expand3_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ idx,
                                const int32_t* d_nk, int64_t N, const float* a_c,
                                const float* b_c, const float* c_c, float* a, float* b,
-                               float* c) {
+                               float* c, const uint8_t* __restrict__ lvalid) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= N) return;
-  if (keep != nullptr && keep[i] == 0) {
+  if (i < N && keep != nullptr && keep[i] == 0) {
     if (a) a[i] = 0.f;
     if (b) b[i] = 0.f;
     if (c) c[i] = 0.f;
   }
-  if (i < *d_nk) {
+  if (i < *d_nk && (lvalid == nullptr || lvalid[i] != 0)) {
     const int r = idx[i];
     if (a) a[r] = a_c[i];
     if (b) b[r] = b_c[i];
@@ -318,7 +359,8 @@ __global__ void scatter_vals_kernel(const float* __restrict__ src, const int32_t
 __global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t* d_nk,
                                  int chunk_index, int chunk_rows, int H, int tile_m, int workers,
                                  int num_kb, int max_split, int fill_pct,
-                                 const int32_t* __restrict__ idx, uint2* __restrict__ dhidden) {
+                                 const int32_t* __restrict__ idx,
+                                 const uint8_t* __restrict__ lvalid, uint2* __restrict__ dhidden) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   if (rows == 0) return;
@@ -332,6 +374,7 @@ __global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t*
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int r = static_cast<int>(g / q);
     const int c = static_cast<int>(g - static_cast<int64_t>(r) * q);
+    if (lvalid != nullptr && lvalid[chunk_start + r] == 0) continue;  // not a kept row
     const int64_t at = static_cast<int64_t>(r) * q + c;
     // all partial loads in flight before the (fixed-order) sum
     float4 v[4];
@@ -385,6 +428,22 @@ cudaError_t launch_compact(const uint8_t* keep, const int64_t* targets, int64_t 
   return cudaGetLastError();
 }
 
+cudaError_t launch_tile_scan(const uint8_t* keep, const int64_t* targets, int64_t N,
+                             int64_t V_valid, int64_t t_offset, uint8_t* tile_flags,
+                             int32_t* tile_list, int32_t* d_na, int32_t* counts, int32_t* idx,
+                             int32_t* targets_c, uint8_t* lvalid, int32_t* d_nk, int* status,
+                             cudaStream_t s) {
+  const int64_t T = (N + 255) / 256;
+  tile_flags_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(keep, N, tile_flags);
+  cudaError_t e = launch_compact(tile_flags, nullptr, T, 1, 0, tile_list, nullptr, d_na, counts,
+                                 status, s);
+  if (e != cudaSuccess) return e;
+  tile_rows_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(keep, targets, N, V_valid, t_offset,
+                                                             tile_list, d_na, idx, targets_c,
+                                                             lvalid, d_nk, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
                                const int32_t* d_nk, int chunk_index, int chunk_rows, int H,
                                __nv_bfloat16* hc, cudaStream_t s) {
@@ -421,8 +480,10 @@ cudaError_t launch_expand4(const uint8_t* keep, const int32_t* idx, const int32_
 
 cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,
                            int64_t N, const float* a_c, const float* b_c, const float* c_c,
-                           float* a, float* b, float* c, cudaStream_t s) {
-  expand3_kernel<<<blocks_for(N, 256), 256, 0, s>>>(keep, idx, d_nk, N, a_c, b_c, c_c, a, b, c);
+                           float* a, float* b, float* c, const uint8_t* lvalid, cudaStream_t s) {
+  // compact rows may reach N rounded up to 256 in block-sparse mode
+  expand3_kernel<<<blocks_for((N + 255) / 256 * 256, 256), 256, 0, s>>>(
+      keep, idx, d_nk, N, a_c, b_c, c_c, a, b, c, lvalid);
   return cudaGetLastError();
 }
 
@@ -437,14 +498,15 @@ cudaError_t launch_expand(const float* src, const int32_t* idx, const int32_t* d
 cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N, const float* a,
                               const float* b, const float* c, const float* d, float* a_c,
                               float* b_c, float* c_c, float* d_c, cudaStream_t s) {
-  gather_vec_kernel<<<blocks_for(N, 256), 256, 0, s>>>(idx, d_nk, a, b, c, d, a_c, b_c, c_c, d_c);
+  gather_vec_kernel<<<blocks_for((N + 255) / 256 * 256, 256), 256, 0, s>>>(idx, d_nk, a, b, c, d,
+                                                                         a_c, b_c, c_c, d_c);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
                              int chunk_rows, int H, int tile_m, int workers, int num_kb,
                              int max_split, int fill_pct, const int32_t* idx,
-                             __nv_bfloat16* dhidden, cudaStream_t s) {
+                             const uint8_t* lvalid, __nv_bfloat16* dhidden, cudaStream_t s) {
   // a grid-stride loop over a grid of 4 blocks per SM: cheap when the
   // contraction was not split and the kernel returns at once
   const int64_t threads = static_cast<int64_t>(chunk_rows) * (H / 4);
@@ -452,7 +514,7 @@ cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_i
   const unsigned cap = static_cast<unsigned>(4 * (device_sm_count() > 0 ? device_sm_count() : 148));
   dh_reduce_kernel<<<want < cap ? want : cap, 256, 0, s>>>(
       reinterpret_cast<const float4*>(part), d_nk, chunk_index, chunk_rows, H, tile_m, workers,
-      num_kb, max_split, fill_pct, idx, reinterpret_cast<uint2*>(dhidden));
+      num_kb, max_split, fill_pct, idx, lvalid, reinterpret_cast<uint2*>(dhidden));
   return cudaGetLastError();
 }
 

@@ -138,7 +138,8 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
       p.part[static_cast<int64_t>(nt) * p.chunk_rows + row] =
           make_float4(m2 * kLn2, s, u2 * kLn2, tz);
   } else if (MODE == kDz) {
-    const bool row_ok = row < rows_valid;
+    // (block-sparse: rows of an active tile that are not kept get dz = 0)
+    const bool row_ok = row < rows_valid && (p.lvalid == nullptr || p.lvalid[cstart + row] != 0);
     float lse2 = 0.f, ca = 0.f, cb = 0.f, glp = 0.f;
     int y = -1;
     if (row_ok) {
@@ -192,7 +193,7 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
                               packed[4 * v + 3]);
     }
   } else if (MODE == kDh) {
-    const bool row_ok = row < rows_valid;
+    const bool row_ok = row < rows_valid && (p.lvalid == nullptr || p.lvalid[cstart + row] != 0);
     const int64_t orow = row_ok ? p.idx[cstart + row] : 0;
     __nv_bfloat16* hrow = p.dhidden + orow * p.H;
     float* prow = p.dh_part +

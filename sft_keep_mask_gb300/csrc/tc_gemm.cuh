@@ -115,13 +115,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tma_load_2d(a_dst, &tma_a, &full[stage], mt * kBM, k0);
             tma_load_2d(a_dst + 8192, &tma_a, &full[stage], mt * kBM + 64, k0);
           } else {
-            tma_load_2d(a_dst, &tma_a, &full[stage], k0, mt * kBM);
+            const int ay = (MODE != kDh && p.tile_list != nullptr)
+                               ? sparse_row(p.tile_list, cstart, mt * kBM) : mt * kBM;
+            tma_load_2d(a_dst, &tma_a, &full[stage], k0, ay);
           }
           if (MODE == kDh || MODE == kDw) {
             // B MN-major: [k rows, n cols]; four 64-column boxes
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              tma_load_2d(b_dst + j * 8192, &tma_b, &full[stage], nt * kBN + 64 * j, k0);
+              tma_load_2d(b_dst + j * 8192, &tma_b, &full[stage], nt * kBN + 64 * j,
+                          (MODE == kDw && p.tile_list != nullptr)
+                              ? sparse_row(p.tile_list, cstart, k0) : k0);
           } else {
             tma_load_2d(b_dst, &tma_b, &full[stage], k0, nt * kBN);
           }

@@ -120,11 +120,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             tma_load_2d_pair(a_dst, &tma_a, bar, m0, k0, pol_a, ha);
             tma_load_2d_pair(a_dst + 8192, &tma_a, bar, m0 + 64, k0, pol_a, ha);
           } else {
-            tma_load_2d_pair(a_dst, &tma_a, bar, k0, m0, pol_a, ha);
+            // block-sparse: the compact rows are read in place from hidden
+            const int ay = (MODE != kDh && p.tile_list != nullptr)
+                               ? sparse_row(p.tile_list, cstart, m0) : m0;
+            tma_load_2d_pair(a_dst, &tma_a, bar, k0, ay, pol_a, ha);
           }
           if (MODE == kDh || MODE == kDw) {
-            tma_load_2d_pair(b_dst, &tma_b, bar, n0, k0, pol_b, hb);
-            tma_load_2d_pair(b_dst + 8192, &tma_b, bar, n0 + 64, k0, pol_b, hb);
+            const int by = (MODE == kDw && p.tile_list != nullptr)
+                               ? sparse_row(p.tile_list, cstart, k0) : k0;
+            tma_load_2d_pair(b_dst, &tma_b, bar, n0, by, pol_b, hb);
+            tma_load_2d_pair(b_dst + 8192, &tma_b, bar, n0 + 64, by, pol_b, hb);
           } else {
             tma_load_2d_pair(b_dst, &tma_b, bar, k0, n0, pol_b, hb);
           }

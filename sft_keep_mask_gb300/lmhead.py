@@ -45,6 +45,10 @@ _SIGS = {
     "lmhead_bwd": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                           _I32, _I32, _VP, ctypes.c_size_t, _VP]),
     "lmhead_expand": (_I32, [_VP, _VP, _VP, _I64, _VP, _VP]),
+    "lmhead_fwd_blocksparse": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _VP, _VP, _VP,
+                                      _I32, _VP, ctypes.c_size_t, _VP]),
+    "lmhead_bwd_blocksparse": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
+                                      _VP, _VP, _I32, _I32, _VP, ctypes.c_size_t, _VP]),
     "lmhead_fwd_shard": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I64, _I64, _I32, _VP, _I32,
                                 _VP, ctypes.c_size_t, _VP]),
     "lmhead_merge_shards": (_I32, [_VP, _I32, _VP, _I64, _I32, _VP, _VP, _VP, _VP]),
@@ -149,7 +153,7 @@ def lmhead_compact(keep, targets, V, idx, targets_c, d_nk, workspace, stream=Non
 
 
 def lmhead_fwd(hidden, weight, targets, keep, want_entropy, logprob, entropy, lse, workspace,
-               chunk_rows=0, stream=None):
+               chunk_rows=0, stream=None, _entry="lmhead_fwd"):
     N, H = hidden.shape
     V = weight.shape[0]
     _need(hidden, torch.bfloat16, "hidden")
@@ -160,14 +164,14 @@ def lmhead_fwd(hidden, weight, targets, keep, want_entropy, logprob, entropy, ls
     _need(entropy, torch.float32, "entropy", N)
     _need(lse, torch.float32, "lse", N)
     _need(workspace, torch.uint8, "workspace")
-    code = lib().lmhead_fwd(_p(hidden), _p(weight), _p(targets), _p(keep), N, H, V,
-                            int(bool(want_entropy)), _p(logprob), _p(entropy), _p(lse),
-                            int(chunk_rows), _p(workspace), workspace.numel(), _s(stream))
-    _check(code, "lmhead_fwd")
+    code = getattr(lib(), _entry)(_p(hidden), _p(weight), _p(targets), _p(keep), N, H, V,
+                                  int(bool(want_entropy)), _p(logprob), _p(entropy), _p(lse),
+                                  int(chunk_rows), _p(workspace), workspace.numel(), _s(stream))
+    _check(code, _entry)
 
 
 def lmhead_bwd(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_entropy, dhidden,
-               dweight, dw_accumulate, workspace, chunk_rows=0, stream=None):
+               dweight, dw_accumulate, workspace, chunk_rows=0, stream=None, _entry="lmhead_bwd"):
     N, H = hidden.shape
     V = weight.shape[0]
     _need(hidden, torch.bfloat16, "hidden")
@@ -181,11 +185,25 @@ def lmhead_bwd(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_e
     _need(dhidden, torch.bfloat16, "dhidden", N * H)
     _need(dweight, torch.float32, "dweight", V * H)
     _need(workspace, torch.uint8, "workspace")
-    code = lib().lmhead_bwd(_p(hidden), _p(weight), _p(targets), _p(keep), N, H, V, _p(lse),
-                            _p(entropy), _p(grad_logprob), _p(grad_entropy), _p(dhidden),
-                            _p(dweight), int(bool(dw_accumulate)), int(chunk_rows),
-                            _p(workspace), workspace.numel(), _s(stream))
-    _check(code, "lmhead_bwd")
+    code = getattr(lib(), _entry)(_p(hidden), _p(weight), _p(targets), _p(keep), N, H, V,
+                                  _p(lse), _p(entropy), _p(grad_logprob), _p(grad_entropy),
+                                  _p(dhidden), _p(dweight), int(bool(dw_accumulate)),
+                                  int(chunk_rows), _p(workspace), workspace.numel(), _s(stream))
+    _check(code, _entry)
+
+
+def lmhead_fwd_blocksparse(hidden, weight, targets, keep, want_entropy, logprob, entropy, lse,
+                           workspace, chunk_rows=0, stream=None):
+    lmhead_fwd(hidden, weight, targets, keep, want_entropy, logprob, entropy, lse, workspace,
+               chunk_rows, stream, _entry="lmhead_fwd_blocksparse")
+
+
+def lmhead_bwd_blocksparse(hidden, weight, targets, keep, lse, entropy, grad_logprob,
+                           grad_entropy, dhidden, dweight, dw_accumulate, workspace, chunk_rows=0,
+                           stream=None):
+    lmhead_bwd(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_entropy, dhidden,
+               dweight, dw_accumulate, workspace, chunk_rows, stream,
+               _entry="lmhead_bwd_blocksparse")
 
 
 def lmhead_fwd_shard(hidden, weight_shard, v_begin, V_total, targets, keep, want_entropy,

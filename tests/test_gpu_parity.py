@@ -24,9 +24,9 @@ DEV = "cuda"
 
 
 def _run_both(w, chunk_rows=0, want_entropy=True, grad_entropy=True, keep_override="auto",
-              accumulate=False, check_bwd=True):
-    inp = synth.make_inputs(w, device=DEV)
-    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=chunk_rows)
+              accumulate=False, check_bwd=True, blocksparse=False, active_frac=1.0):
+    inp = synth.make_inputs(w, device=DEV, active_frac=active_frac)
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=chunk_rows, blocksparse=blocksparse)
     if isinstance(keep_override, str):
         keep = gpu_keep(sc, inp)
         keep_np = oracle_keep(inp)
@@ -332,3 +332,47 @@ def test_tiny_and_degenerate_shapes(monkeypatch, variant, N, H, V):
         keep = np.zeros(N, np.uint8)
         keep[::2] = 1
         _run_both(w, keep_override=keep)
+
+
+# ------------------------------------------------ block-sparse tile skipping
+
+@pytest.mark.parametrize("variant", ["pair", "single"])
+def test_blocksparse_matches_the_oracle(monkeypatch, variant):
+    monkeypatch.setenv("LMHEAD_GEMM", variant)
+    # contiguous active suffixes (the entropy-bonus layout), ragged H and V,
+    # several chunks of active tiles
+    w = synth.workload("entropy_bonus", N=5000, H=320, V=3001)
+    _run_both(w, chunk_rows=512, blocksparse=True, active_frac=0.4)
+    # scattered keep mask: almost every tile is active
+    _run_both(synth.workload("tiny", seed=140, N=700, H=192, V=1500), blocksparse=True)
+
+
+def test_blocksparse_edge_cases():
+    w = synth.workload("tiny", seed=141, N=300, H=64, V=700)
+    _run_both(w, keep_override=None, blocksparse=True)
+    _run_both(w, keep_override=np.zeros(300, np.uint8), blocksparse=True)
+    one = np.zeros(300, np.uint8)
+    one[299] = 1  # a kept row in the last, partial tile
+    _run_both(w, keep_override=one, blocksparse=True, chunk_rows=256)
+
+
+def test_blocksparse_forward_equals_compaction_bitwise():
+    # a row's logits accumulate in the same order wherever the row sits, so
+    # the forward results of the two strategies agree bit for bit
+    w = synth.workload("entropy_bonus", N=6144, H=256, V=4000)
+    inp = synth.make_inputs(w, device=DEV, active_frac=0.7)
+    outs = []
+    for bs in (False, True):
+        sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=1024, blocksparse=bs)
+        keep = gpu_keep(sc, inp)
+        lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+        dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                             inp["grad_logprob"], inp["grad_entropy"])
+        torch.cuda.synchronize()
+        assert sc.status() == 0
+        outs.append((lp, ent, lse, dh, dW))
+    (a, b) = outs
+    for x, y in zip(a[:3], b[:3]):
+        assert torch.equal(x, y)
+    assert torch.allclose(a[3].float(), b[3].float(), rtol=2e-2, atol=1e-3)
+    assert torch.allclose(a[4], b[4], rtol=1e-4, atol=1e-5)
