@@ -262,7 +262,8 @@ def run_ours(args):
     w = _workload(args)
     w = synth.workload(args.workload, N=w.N, V=w.V, seed=w.seed + 100 * rank)
     inp = synth.make_inputs(w, device=dev, active_frac=args.active_frac)
-    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=args.chunk_rows, device=dev)
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=args.chunk_rows, device=dev,
+                      blocksparse=args.blocksparse)
     comps = inp.get("components")
     lens = inp.get("seq_lens")
     offsets = None
@@ -292,11 +293,13 @@ def run_ours(args):
             L.lmhead_build_keep_mask(loss_mask, None, None, offs, keep, stream)
         else:
             keep.copy_(inp["keep"])
-        L.lmhead_fwd(hidden, inp["weight"], targets, keep_arg, True, lp, ent, lse, ws,
-                     args.chunk_rows, stream)
+        fwd = L.lmhead_fwd_blocksparse if args.blocksparse else L.lmhead_fwd
+        bwd = L.lmhead_bwd_blocksparse if args.blocksparse else L.lmhead_bwd
+        fwd(hidden, inp["weight"], targets, keep_arg, True, lp, ent, lse, ws, args.chunk_rows,
+            stream)
         if args.mode == "fwdbwd":
-            L.lmhead_bwd(hidden, inp["weight"], targets, keep_arg, lse, ent, g_lp, g_e, dh, dW,
-                         False, ws, args.chunk_rows, stream)
+            bwd(hidden, inp["weight"], targets, keep_arg, lse, ent, g_lp, g_e, dh, dW, False, ws,
+                args.chunk_rows, stream)
 
     loss_mask = comps[0] if comps is not None else None
     dev_args = (inp["hidden"], inp["targets"], loss_mask, offsets, inp["grad_logprob"], g_ent)
@@ -408,6 +411,7 @@ def run_ours(args):
                        "kept_frac": nk / N, "chunk_rows": args.chunk_rows or 8192,
                        "entropy": "differentiable" if g_ent is not None else "metric-only",
                        "mode": args.mode, "keep_mask": "off" if args.keep_off else "on",
+                       "rows": "block-sparse tiles" if args.blocksparse else "compacted",
                        "l2": "inputs larger than L2 (W 1.2 GB, hidden 0.5 GB)",
                        "parallelism": f"replicas x{world}"},
             "peak_device_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
@@ -511,6 +515,8 @@ def main():
     ap.add_argument("--mode", default="fwdbwd", choices=["fwdbwd", "fwd"])
     ap.add_argument("--keep-off", action="store_true",
                     help="score every row (keep mask off), the comparison arm")
+    ap.add_argument("--blocksparse", action="store_true",
+                    help="score the active 256-row tiles in place instead of compacting")
     ap.add_argument("--active-frac", type=float, default=1.0,
                     help="active suffix fraction of the entropy_bonus workload")
     ap.add_argument("--ref-rows", type=int, default=256)
