@@ -223,13 +223,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int MODE>
 cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                            const TcGemmParams& p, int grid, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGemmSmemBytes);
+  // the shared-memory opt-in is per device: set it once on each device used
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   tc_gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(tma_a, tma_b, p);
   return cudaGetLastError();

@@ -232,13 +232,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 template <int MODE>
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                                 const TcGemmParams& p, int grid, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kPairSmemBytes);
+  // the shared-memory opt-in is per device: set it once on each device used
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   tc_gemm_pair_kernel<MODE><<<grid, kGemmThreads, kPairSmemBytes, stream>>>(tma_a, tma_b, p);
   return cudaGetLastError();

@@ -376,3 +376,32 @@ def test_blocksparse_forward_equals_compaction_bitwise():
         assert torch.equal(x, y)
     assert torch.allclose(a[3].float(), b[3].float(), rtol=2e-2, atol=1e-3)
     assert torch.allclose(a[4], b[4], rtol=1e-4, atol=1e-5)
+
+
+def _full_size_fwd_bwd(w, active_frac=1.0, rows=16):
+    inp = synth.make_inputs(w, device=DEV, active_frac=active_frac)
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    keep = gpu_keep(sc, inp)
+    np.testing.assert_array_equal(keep.cpu().numpy(), oracle_keep(inp))
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+    dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                         inp["grad_logprob"], inp["grad_entropy"])
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    _sampled_rows_check(w, inp, keep, dict(lp=lp, ent=ent, lse=lse, dh=dh), rows, True)
+    k = keep.bool()
+    assert (lp[~k] == 0).all() and (dh[~k] == 0).all()
+    col = dW.double().sum(0)
+    assert col.abs().max().item() <= 1e-3 * dW.double().abs().sum(0).max().item()
+
+
+def test_full_size_entropy_bonus_sampled():
+    _full_size_fwd_bwd(synth.workload("entropy_bonus"), active_frac=0.64)
+
+
+def test_full_size_long_context_sampled():
+    # the largest workload: N = 262144 rows, H = 5120; no [N, V] buffer exists
+    w = synth.workload("long_context")
+    torch.cuda.reset_peak_memory_stats()
+    _full_size_fwd_bwd(w, rows=12)
+    assert torch.cuda.max_memory_allocated() < 0.25 * w.N * w.V * 2
