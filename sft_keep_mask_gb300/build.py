@@ -72,6 +72,24 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     return LIB
 
 
+EXAMPLE_SRC = os.path.join(PKG, "examples", "lmhead_c_example.c")
+EXAMPLE_BIN = os.path.join(BUILD, "lmhead_c_example")
+
+
+def build_example() -> str:
+    """Compile the plain-C example caller of the C ABI against liblmhead.so."""
+    lib = build()
+    cuda_home = os.path.dirname(os.path.dirname(_nvcc()))
+    cmd = ["gcc", "-O2", "-std=c11", EXAMPLE_SRC, "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(cuda_home, "include"), "-L", LIBDIR, "-llmhead",
+           f"-Wl,-rpath,{LIBDIR}", "-L", os.path.join(cuda_home, "lib64"), "-lcudart", "-lm",
+           f"-Wl,-rpath,{os.path.join(cuda_home, 'lib64')}", "-o", EXAMPLE_BIN]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"example build failed:\n{r.stdout}\n{r.stderr}")
+    return EXAMPLE_BIN
+
+
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,

@@ -414,3 +414,27 @@ def test_full_size_long_context_sampled():
     outputs = w.N * 4 * 3 + w.N * w.H * 2 + w.V * w.H * 4
     assert added <= outputs + (1 << 20)
     assert added < 0.1 * w.N * w.V * 2
+
+
+def test_random_shape_sweep():
+    # seeded random problems: shapes, keep densities, chunk sizes, GEMM
+    # variant and strategy all vary; every one must match the oracle
+    rng = np.random.default_rng(2026)
+    import os
+    for case in range(12):
+        N = int(rng.integers(1, 1500))
+        H = int(rng.choice([8, 16, 64, 136, 256, 520]))
+        V = int(rng.integers(1, 4200))
+        chunk = int(rng.choice([0, 256, 512, 768]))
+        density = float(rng.choice([0.0, 0.05, 0.5, 1.0]))
+        keep = (rng.random(N) < density).astype(np.uint8)
+        variant = str(rng.choice(["pair", "single"]))
+        bs = bool(rng.integers(0, 2))
+        ent = bool(rng.integers(0, 2))
+        os.environ["LMHEAD_GEMM"] = variant
+        try:
+            w = synth.workload("tiny", seed=300 + case, N=N, H=H, V=V)
+            _run_both(w, chunk_rows=chunk, keep_override=keep, blocksparse=bs,
+                      grad_entropy=ent)
+        finally:
+            del os.environ["LMHEAD_GEMM"]

@@ -100,3 +100,14 @@ def test_step_pipeline_overlapped_copies_give_the_same_results():
     assert torch.equal(out[0], direct[-1][0]) and torch.equal(out[1], direct[-1][1])
     for (a, b), (c, d) in zip(seen, direct):
         assert torch.equal(a, c) and torch.equal(b, d)
+
+
+def test_plain_c_caller():
+    # the C ABI used from C alone: cudaMalloc'd buffers, lmhead_fwd /
+    # lmhead_bwd, property checks on the results (see the example's header)
+    import subprocess
+    from sft_keep_mask_gb300 import build as b
+    exe = b.build_example()
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "0 bad rows" in r.stdout
