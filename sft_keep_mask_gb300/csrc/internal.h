@@ -32,7 +32,8 @@ struct TcGemmParams {
   int chunk_rows;           // C: most rows per chunk (multiple of 256)
   int V;
   int H;
-  int group_n;              // N tiles per raster group (L2 reuse)
+  int group_m;              // M tiles per raster block, 0 = none (see tile_coords)
+  int group_n;              // N tiles per raster group when group_m == 0
   int hint_a;               // L2 policy of A / B loads (CTA pairs): 0 none,
   int hint_b;               //   1 evict first, 2 evict last, 3 evict normal
   int* status;              // device status word
@@ -76,7 +77,7 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma
 // cost of the weight-gradient update stays hidden behind its MMAs).  Chunk c
 // covers compact rows [start, start + rows); rows == 0 past the last chunk.
 // Computed on the device from Nk, so the host never waits for Nk.
-__device__ __forceinline__ void chunk_span(int nk, int C, int c, int& start, int& rows) {
+__host__ __device__ __forceinline__ void chunk_span(int nk, int C, int c, int& start, int& rows) {
   if (nk <= 0) {
     start = 0;
     rows = 0;

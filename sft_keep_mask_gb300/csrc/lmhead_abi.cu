@@ -22,7 +22,11 @@ namespace {
 constexpr bool kDefaultPair = true;
 constexpr int kDhMaxSplit = 4;  // largest K split of the dHidden contraction
 static_assert(kDhMaxSplit <= 4, "the dHidden reduction sums at most four partials");
-constexpr int kDhSplitFillPct = 85;  // split only when fewer worker slots than this are busy
+constexpr int kDhSplitFillPct = 85;
+// Rows of Hc per raster block of the vocabulary projections (kFwd, kDz): 32 MB
+// of bf16 rows at H = 4096, small enough to stay in L2 (together with the
+// vocabulary tiles in flight) while W streams past once per block.
+constexpr int kRowBlockRows = 4096;  // split only when fewer worker slots than this are busy
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 inline int64_t cdiv(int64_t x, int64_t m) { return (x + m - 1) / m; }
@@ -352,6 +356,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.chunk_rows = static_cast<int>(L.C);
   p.V = V;
   p.H = H;
+  p.group_m = kRowBlockRows / (pair ? 256 : kBM);
   p.group_n = 16;
   p.status = status;
   p.stall = fault_at("stall") ? 1 : 0;
@@ -507,11 +512,13 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     }
     {
       Launch l(kKindGemmDz, s);
+      p.group_m = kRowBlockRows / (pair ? 256 : kBM);
       p.group_n = 16;
       LM_TRY(run_gemm<kDz>(pair, m_hc_k, m_w_k, m_w_k2, p, L.C, V, s));
     }
     {
       Launch l(kKindGemmDh, s);
+      p.group_m = 0;
       p.group_n = static_cast<int>(n_h_tiles);
       LM_TRY(run_gemm<kDh>(pair, m_dz_k, m_w_mn, m_w_mn, p, L.C, H, s, &dh_workers));
     }
@@ -524,6 +531,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     }
     {
       Launch l(kKindGemmDw, s);
+      p.group_m = 0;
       p.group_n = static_cast<int>(n_h_tiles);
       p.beta = (c > 0 || dw_accumulate) ? 1 : 0;
       LM_TRY(run_gemm<kDw>(pair, m_dz_mn, m_hc_mn, m_hc_mn, p, V, H, s));

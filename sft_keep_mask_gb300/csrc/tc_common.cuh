@@ -27,11 +27,28 @@ namespace lmhead {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Tile t -> (row tile, column tile).  Tiles walk `group_n` column tiles for
-// every row tile before the next group, so the CTAs in flight share the
-// group's column operand through L2.
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_n, int& mt,
-                                            int& nt) {
+// Tile t -> (row tile, column tile).
+//
+// group_m > 0 (the vocabulary projections): the row tiles form blocks of
+// group_m; inside a block the tiles walk the block's row tiles for every
+// column tile.  The block's A rows (group_m x 256 rows of Hc) stay in L2 while
+// the column operand (W) streams past once per block.
+//
+// group_m == 0: tiles walk `group_n` column tiles for every row tile before
+// the next group, so the CTAs in flight share the group's column operand
+// through L2 (dHidden, dW: group_n = all of H).
+__host__ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m,
+                                                     int group_n, int& mt, int& nt) {
+  if (group_m > 0) {
+    const int per_block = group_m * num_n;
+    const int b = t / per_block;
+    const int local = t - b * per_block;
+    const int left = num_m - b * group_m;
+    const int rows = left < group_m ? left : group_m;
+    nt = local / rows;
+    mt = b * group_m + (local - nt * rows);
+    return;
+  }
   const int per_group = num_m * group_n;
   const int g = t / per_group;
   const int local = t - g * per_group;

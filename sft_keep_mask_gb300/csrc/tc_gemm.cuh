@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
         const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
         int mt, nt;
-        tile_coords(t, num_m, num_n, p.group_n, mt, nt);
+        tile_coords(t, num_m, num_n, p.group_m, p.group_n, mt, nt);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int t = u % num_tiles;
       const int sidx = u / num_tiles;
       int mt, nt;
-      tile_coords(t, num_m, num_n, p.group_n, mt, nt);
+      tile_coords(t, num_m, num_n, p.group_m, p.group_n, mt, nt);
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       if (num_kb > 0) {

@@ -1,0 +1,78 @@
+// Host-side check of the persistent GEMMs' work schedule (no GPU needed):
+//   * tile_coords maps the tile indices 0 .. num_m*num_n-1 one-to-one onto
+//     the (row tile, column tile) grid for every raster setting in use;
+//   * chunk_span splits Nk kept rows into chunks that cover [0, Nk) in order,
+//     each at most chunk_rows long;
+//   * dh_split_count never splits past the K blocks or the partial buffers.
+// Prints "ok" and exits 0, or names the first failing case and exits 1.
+#include <cstdio>
+#include <vector>
+
+#include "../../sft_keep_mask_gb300/csrc/tc_common.cuh"
+
+using namespace lmhead;
+
+static int check_raster(int num_m, int num_n, int group_m, int group_n) {
+  std::vector<int> seen(static_cast<size_t>(num_m) * num_n, 0);
+  for (int t = 0; t < num_m * num_n; ++t) {
+    int mt = -1, nt = -1;
+    tile_coords(t, num_m, num_n, group_m, group_n, mt, nt);
+    if (mt < 0 || mt >= num_m || nt < 0 || nt >= num_n) {
+      std::printf("raster out of range: M=%d N=%d gm=%d gn=%d t=%d -> (%d,%d)\n", num_m, num_n,
+                  group_m, group_n, t, mt, nt);
+      return 1;
+    }
+    if (seen[static_cast<size_t>(mt) * num_n + nt]++) {
+      std::printf("raster repeats a tile: M=%d N=%d gm=%d gn=%d t=%d\n", num_m, num_n, group_m,
+                  group_n, t);
+      return 1;
+    }
+  }
+  return 0;
+}
+
+int main() {
+  const int ms[] = {1, 2, 3, 15, 16, 17, 29, 32, 33, 64, 257};
+  const int ns[] = {1, 2, 5, 16, 17, 40, 594};
+  const int gms[] = {0, 1, 3, 8, 16, 32};
+  const int gns[] = {1, 4, 16, 64};
+  for (int m : ms)
+    for (int n : ns)
+      for (int gm : gms)
+        for (int gn : gns)
+          if (check_raster(m, n, gm, gn)) return 1;
+
+  const int nks[] = {0, 1, 255, 256, 257, 8191, 8192, 8193, 36258, 65536, 100000};
+  const int cs[] = {256, 2048, 8192};
+  for (int nk : nks)
+    for (int c : cs) {
+      const int slots = (nk + c - 1) / c + 1;
+      int next = 0;
+      for (int i = 0; i < slots + 2; ++i) {
+        int start = -1, rows = -1;
+        chunk_span(nk, c, i, start, rows);
+        if (rows < 0 || rows > c || (rows > 0 && start != next)) {
+          std::printf("chunk_span: Nk=%d C=%d chunk %d -> start %d rows %d (expected start %d)\n",
+                      nk, c, i, start, rows, next);
+          return 1;
+        }
+        next += rows;
+      }
+      if (next != nk) {
+        std::printf("chunk_span: Nk=%d C=%d covers %d rows\n", nk, c, next);
+        return 1;
+      }
+    }
+
+  for (int tiles = 1; tiles < 700; tiles += 7)
+    for (int workers : {1, 38, 76, 152})
+      for (int kb : {1, 2, 3, 64, 2374}) {
+        const int s = dh_split_count(tiles, workers, kb, 4, 85);
+        if (s < 1 || s > 4 || s > kb) {
+          std::printf("dh_split_count(%d, %d, %d) = %d\n", tiles, workers, kb, s);
+          return 1;
+        }
+      }
+  std::printf("ok\n");
+  return 0;
+}
