@@ -46,14 +46,23 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Longest time one try_wait may keep the calling thread suspended while the
+// phase is incomplete.  The thread resumes as soon as the phase completes, so
+// this bounds only the sleep between polls: with an explicit hint the idle
+// waiters (epilogue warps during the MMAs, producer and issuer between stages)
+// sleep instead of re-polling, which left more of the power budget to the
+// tensor cores (the fwd + bwd step under the power cap ran 2.8% faster with a
+// 2 us or a 200 us hint than with the default limit).
+constexpr uint32_t kTryWaitSuspendNs = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
