@@ -34,8 +34,6 @@ struct TcGemmParams {
   int H;
   int group_m;              // M tiles per raster block, 0 = none (see tile_coords)
   int group_n;              // N tiles per raster group when group_m == 0
-  int hint_a;               // L2 policy of A / B loads (CTA pairs): 0 none,
-  int hint_b;               //   1 evict first, 2 evict last, 3 evict normal
   int* status;              // device status word
   // epilogue operands (compact, indexed by compact row)
   const int32_t* targets_c;

@@ -181,9 +181,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
-// `ld` elements; boxes of [box_rows, box_cols] with the 128-byte swizzle
-// (box_cols * 2 == 128).  Out-of-range elements load as zero.
 // Host-side fault injection for tests: LMHEAD_FAULT names a site --
 //   "tensor_map"  tensor-map encoding fails          (call returns ECUDA)
 //   "launch"      the first GEMM launch is refused    (call returns ECUDA)
@@ -194,6 +191,9 @@ bool fault_at(const char* site) {
   return e != nullptr && std::strcmp(e, site) == 0;
 }
 
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
+// `ld` elements; boxes of [box_rows, box_cols] with the 128-byte swizzle
+// (box_cols * 2 == 128).  Out-of-range elements load as zero.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
               int box_rows, int box_cols) {
   if (fault_at("tensor_map")) return false;

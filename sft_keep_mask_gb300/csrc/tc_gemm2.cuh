@@ -96,9 +96,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       const int half = static_cast<int>(rank) * 128;
-      const uint64_t pol_a = make_l2_policy(p.hint_a);
-      const uint64_t pol_b = make_l2_policy(p.hint_b);
-      const bool ha = p.hint_a != 0, hb = p.hint_b != 0;
       for (int u = pair; u < num_units && !p.stall; u += num_pairs) {
         const int t = u % num_tiles;
         const int sidx = u / num_tiles;
@@ -117,21 +114,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const int m0 = mt * kPairTileM + half;
           const int n0 = nt * kBN + half;
           if (MODE == kDw) {
-            tma_load_2d_pair(a_dst, &tma_a, bar, m0, k0, pol_a, ha);
-            tma_load_2d_pair(a_dst + 8192, &tma_a, bar, m0 + 64, k0, pol_a, ha);
+            tma_load_2d_pair(a_dst, &tma_a, bar, m0, k0);
+            tma_load_2d_pair(a_dst + 8192, &tma_a, bar, m0 + 64, k0);
           } else {
             // block-sparse: the compact rows are read in place from hidden
             const int ay = (MODE != kDh && p.tile_list != nullptr)
                                ? sparse_row(p.tile_list, cstart, m0) : m0;
-            tma_load_2d_pair(a_dst, &tma_a, bar, k0, ay, pol_a, ha);
+            tma_load_2d_pair(a_dst, &tma_a, bar, k0, ay);
           }
           if (MODE == kDh || MODE == kDw) {
             const int by = (MODE == kDw && p.tile_list != nullptr)
                                ? sparse_row(p.tile_list, cstart, k0) : k0;
-            tma_load_2d_pair(b_dst, &tma_b, bar, n0, by, pol_b, hb);
-            tma_load_2d_pair(b_dst + 8192, &tma_b, bar, n0 + 64, by, pol_b, hb);
+            tma_load_2d_pair(b_dst, &tma_b, bar, n0, by);
+            tma_load_2d_pair(b_dst + 8192, &tma_b, bar, n0 + 64, by);
           } else {
-            tma_load_2d_pair(b_dst, &tma_b, bar, k0, n0, pol_b, hb);
+            tma_load_2d_pair(b_dst, &tma_b, bar, k0, n0);
           }
           ++issued;
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
