@@ -2,9 +2,13 @@
 
 The compute path is the CUDA library ``_lib/liblmhead.so`` (sources in
 ``csrc/``, C ABI in ``include/lmhead.h``); ``lmhead`` is its thin ctypes
-binding and ``api`` a small convenience layer that allocates outputs and the
-workspace with torch.  ``synth`` draws seeded synthetic inputs.
+binding, ``api`` a small convenience layer that allocates outputs and the
+workspace with torch, and ``autograd`` the op ``hidden_to_logprobs`` (forward
+and backward through the library under torch autograd).  ``synth`` draws
+seeded synthetic inputs.
 """
+
+from .autograd import hidden_to_logprobs  # noqa: F401
 
 from .lmhead import (  # noqa: F401
     DEFAULT_CHUNK_ROWS,

@@ -120,3 +120,17 @@ def test_binding_refuses_a_missing_library(monkeypatch, tmp_path):
     monkeypatch.setattr(lmhead, "_LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
         lmhead.lib()
+
+
+def test_autograd_op_rejects_bad_arguments_before_any_call():
+    import torch
+    from sft_keep_mask_gb300 import hidden_to_logprobs
+    h = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(16, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError, match="return_entropy"):
+        hidden_to_logprobs(h, W, y, entropy_requires_grad=True)
+    with pytest.raises(TypeError, match="main_grad"):
+        hidden_to_logprobs(h, W, y, main_grad=torch.zeros(16, 8, dtype=torch.bfloat16))
+    with pytest.raises(TypeError, match="main_grad"):
+        hidden_to_logprobs(h, W, y, main_grad=torch.zeros(8, 16))
