@@ -5,8 +5,8 @@
 #include "tc_gemm2.cuh"
 
 namespace lmhead {
-template cudaError_t launch_tc_gemm<kDz>(const CUtensorMap&, const CUtensorMap&,
+template cudaError_t launch_tc_gemm<kDz>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                            const TcGemmParams&, int, cudaStream_t);
-template cudaError_t launch_tc_gemm_pair<kDz>(const CUtensorMap&, const CUtensorMap&,
+template cudaError_t launch_tc_gemm_pair<kDz>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                 const TcGemmParams&, int, cudaStream_t);
 }  // namespace lmhead

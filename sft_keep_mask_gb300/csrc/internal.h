@@ -17,7 +17,6 @@ constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kGemmSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256;
 
 // The four contractions of the path.
 //   kFwd: Z = Hc W^T  -> per-row online-softmax partials per 256-column tile
@@ -25,6 +24,18 @@ constexpr int kGemmSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256;
 //   kDh : dHc = dZ W  -> rows scattered to dhidden (bf16)
 //   kDw : dW (+)= dZ^T Hc (fp32)
 enum GemmMode : int { kFwd = 0, kDz = 1, kDh = 2, kDw = 3 };
+
+// Output staging of the kDz / kDw epilogues: per epilogue warp two 4 KB
+// buffers, each one TMA box of 32 rows x 128 bytes (128-byte swizzle).
+constexpr int kOutBoxBytes = 32 * 128;
+constexpr int kOutStageBytes = 4 * 2 * kOutBoxBytes;
+constexpr int out_stage_bytes(int mode) {
+  return (mode == kDz || mode == kDw) ? kOutStageBytes : 0;
+}
+template <int MODE>
+constexpr int gemm_smem_bytes() {
+  return kStages * (kABytes + kBBytes) + out_stage_bytes(MODE) + 1024 + 256;
+}
 
 struct TcGemmParams {
   const int32_t* d_nk;      // device Nk
@@ -44,11 +55,8 @@ struct TcGemmParams {
   const float* gent_c;      // nullable: metric-only entropy
   int want_entropy;
   float4* part;             // kFwd: [ceil(V/kBN)][C] (m, s, u, t)
-  __nv_bfloat16* dz;        // kDz: [C, dz_ld]
-  int64_t dz_ld;
   __nv_bfloat16* dhidden;   // kDh: [N, H]
-  float* dw;                // kDw: [V, H]
-  int beta;                 // kDw: 1 = add to dw
+  int beta;                 // kDw: 1 = add to dW (the output map's tensor)
   float* dh_part;           // kDh split over K: [max_split][C][H] fp32 partial sums
   int max_split;            // kDh: largest K split (1 = never split)
   int split_fill_pct;       // kDh: split only below this fill of the worker slots
@@ -60,15 +68,20 @@ struct TcGemmParams {
   const uint8_t* lvalid;    // per compact row: 1 if it is a kept row
 };
 
+// tma_c is the output map of kDz (dZ chunk, bf16, boxes of 32 rows x 64
+// columns) and kDw (dW, fp32, boxes of 32 rows x 32 columns), both with the
+// 128-byte swizzle; the other contractions do not read it.
 template <int MODE>
 cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
-                           const TcGemmParams& p, int grid, cudaStream_t stream);
+                           const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
+                           cudaStream_t stream);
 
 // The same contractions on CTA pairs (256 x 256 tiles, cta_group::2); `grid`
 // must be even.  Its B maps use 128-row boxes (each CTA stages half of B).
 template <int MODE>
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
-                                const TcGemmParams& p, int grid, cudaStream_t stream);
+                                const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
+                                cudaStream_t stream);
 
 // The Nk kept rows are cut into ceil(Nk / C) chunks of equal size rounded up
 // to 256 rows (so no chunk is much shorter than the others and the per-chunk

@@ -191,19 +191,22 @@ bool fault_at(const char* site) {
   return e != nullptr && std::strcmp(e, site) == 0;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
-// `ld` elements; boxes of [box_rows, box_cols] with the 128-byte swizzle
-// (box_cols * 2 == 128).  Out-of-range elements load as zero.
+// 2-D tensor map over a row-major [rows, cols] matrix of bf16 (or fp32 with
+// `f32`) with row stride `ld` elements; boxes of [box_rows, box_cols] with the
+// 128-byte swizzle (box_cols * element size == 128).  Loads of out-of-range
+// elements read zero; stores and reductions skip them.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
-              int box_rows, int box_cols) {
+              int box_rows, int box_cols, bool f32 = false) {
   if (fault_at("tensor_map")) return false;
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
+  const int64_t esize = f32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esize)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -283,13 +286,14 @@ bool use_pair() {
 
 // Launches one contraction on the selected variant.  m_upper bounds the rows
 // of D (the chunk for kFwd/kDz/kDh, V for kDw); b_single / b_pair are the B
-// maps for the two variants (they differ only for K-major B).
+// maps for the two variants (they differ only for K-major B); c is the output
+// map of kDz / kDw (the other contractions do not read it).
 // *workers receives the number of persistent workers launched (CTA pairs or
 // CTAs), which the dHidden split rule depends on.
 template <int MODE>
 cudaError_t run_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b_single,
-                     const CUtensorMap& b_pair, const TcGemmParams& p, int64_t m_upper,
-                     int64_t n, cudaStream_t s, int* workers = nullptr) {
+                     const CUtensorMap& b_pair, const CUtensorMap& c, const TcGemmParams& p,
+                     int64_t m_upper, int64_t n, cudaStream_t s, int* workers = nullptr) {
   if (fault_at("launch")) return cudaErrorLaunchFailure;
   const int split = MODE == kDh ? p.max_split : 1;
   if (pair) {
@@ -297,11 +301,11 @@ cudaError_t run_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b_singl
     const int64_t pairs = device_info().sms / 2;
     const int64_t w = tiles < pairs ? (tiles < 1 ? 1 : tiles) : pairs;
     if (workers != nullptr) *workers = static_cast<int>(w);
-    return launch_tc_gemm_pair<MODE>(a, b_pair, p, static_cast<int>(2 * w), s);
+    return launch_tc_gemm_pair<MODE>(a, b_pair, c, p, static_cast<int>(2 * w), s);
   }
   const int grid = gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN) * split);
   if (workers != nullptr) *workers = grid;
-  return launch_tc_gemm<MODE>(a, b_single, p, grid, s);
+  return launch_tc_gemm<MODE>(a, b_single, c, p, grid, s);
 }
 
 // Forward over the vocabulary rows held in `weight` ([V, H]).  For the whole
@@ -389,7 +393,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
     p.chunk_index = static_cast<int>(c);
     {
       Launch l(kKindGemmFwd, s);
-      LM_TRY(run_gemm<kFwd>(pair, ma, mb, mb2, p, L.C, V, s));
+      LM_TRY(run_gemm<kFwd>(pair, ma, mb, mb2, ma, p, L.C, V, s));
     }
     {
       Launch l(kKindMerge, s);
@@ -475,7 +479,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   }
 
   const bool pair = use_pair();
-  CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn;
+  CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn, m_dz_out, m_dw_out;
   const void* rows_src = blocksparse ? hidden : static_cast<const void*>(hc);
   const int64_t rows_n = blocksparse ? N : L.C;
   if (!make_map(&m_hc_k, rows_src, rows_n, H, H, kBM, 64) ||  // A of kDz (K-major)
@@ -484,7 +488,9 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       !make_map(&m_dz_k, dz, L.C, V, L.dz_ld, kBM, 64) ||  // A of kDh (K-major)
       !make_map(&m_w_mn, weight, V, H, H, 64, 64) ||       // B of kDh (MN-major boxes)
       !make_map(&m_dz_mn, dz, L.C, V, L.dz_ld, 64, 64) ||  // A of kDw (MN-major boxes)
-      !make_map(&m_hc_mn, rows_src, rows_n, H, H, 64, 64))  // B of kDw (MN-major boxes)
+      !make_map(&m_hc_mn, rows_src, rows_n, H, H, 64, 64) ||  // B of kDw (MN-major boxes)
+      !make_map(&m_dz_out, dz, L.C, V, L.dz_ld, 32, 64) ||   // output of kDz
+      !make_map(&m_dw_out, dweight, V, H, H, 32, 32, true))   // output of kDw (fp32)
     return LMHEAD_ECUDA;
 
   TcGemmParams p{};
@@ -503,10 +509,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.glp_c = glp_c;
   p.gent_c = grad_entropy ? gent_c : nullptr;
   p.want_entropy = grad_entropy ? 1 : 0;
-  p.dz = dz;
-  p.dz_ld = L.dz_ld;
   p.dhidden = static_cast<__nv_bfloat16*>(dhidden);
-  p.dw = dweight;
   p.dh_part = at<float>(workspace, L.dhp);
   p.max_split = kDhMaxSplit;
   p.split_fill_pct = kDhSplitFillPct;
@@ -526,13 +529,13 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       Launch l(kKindGemmDz, s);
       p.group_m = row_block_tiles(H, pair ? 256 : kBM, L.C);
       p.group_n = 16;
-      LM_TRY(run_gemm<kDz>(pair, m_hc_k, m_w_k, m_w_k2, p, L.C, V, s));
+      LM_TRY(run_gemm<kDz>(pair, m_hc_k, m_w_k, m_w_k2, m_dz_out, p, L.C, V, s));
     }
     {
       Launch l(kKindGemmDh, s);
       p.group_m = 0;
       p.group_n = static_cast<int>(n_h_tiles);
-      LM_TRY(run_gemm<kDh>(pair, m_dz_k, m_w_mn, m_w_mn, p, L.C, H, s, &dh_workers));
+      LM_TRY(run_gemm<kDh>(pair, m_dz_k, m_w_mn, m_w_mn, m_dz_k, p, L.C, H, s, &dh_workers));
     }
     {
       Launch l(kKindDhReduce, s);
@@ -546,7 +549,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       p.group_m = 0;
       p.group_n = static_cast<int>(n_h_tiles);
       p.beta = (c > 0 || dw_accumulate) ? 1 : 0;
-      LM_TRY(run_gemm<kDw>(pair, m_dz_mn, m_hc_mn, m_hc_mn, p, V, H, s));
+      LM_TRY(run_gemm<kDw>(pair, m_dz_mn, m_hc_mn, m_hc_mn, m_dw_out, p, V, H, s));
     }
   }
   return LMHEAD_OK;

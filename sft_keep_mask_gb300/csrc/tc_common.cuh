@@ -71,6 +71,46 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
+// Staged TMA output of one epilogue warp (kDz, kDw).  The warp's 32 rows of
+// a 128-byte-wide box go to one of its two 4 KB buffers in the 128-byte
+// swizzled layout the tensor map expects (16-byte chunk c of row r at chunk
+// position c ^ (r & 7); the buffers are 1024-byte aligned), then lane 0 has
+// the TMA write the box.  A buffer is refilled only after the store issued
+// from it two boxes earlier has read it.
+struct OutStage {
+  const CUtensorMap* map;  // output tensor map (box: 32 rows x 128 bytes)
+  uint8_t* buf;            // this warp's two buffers (8 KB, 1024-byte aligned)
+  uint32_t issued;         // boxes issued by this warp so far
+};
+
+// Buffer for the next box; waits until the store issued from it has read it.
+__device__ __forceinline__ uint8_t* out_buffer(OutStage& os, int lane) {
+  if (lane == 0) bulk_wait_read_all_but_one();
+  __syncwarp();
+  return os.buf + (os.issued & 1u) * kOutBoxBytes;
+}
+
+// 16-byte chunk c (0..7) of this lane's 128-byte row in the buffer.
+__device__ __forceinline__ void out_put(uint8_t* b, int lane, int c, uint4 v) {
+  *reinterpret_cast<uint4*>(b + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+}
+
+// Makes the buffer visible to the TMA and writes (or, with `add`, adds) the
+// box whose top-left element is (x, y) of the output map.
+__device__ __forceinline__ void out_issue(OutStage& os, uint8_t* b, int lane, int x, int y,
+                                          bool add) {
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    if (add)
+      tma_reduce_add_2d(os.map, b, x, y);
+    else
+      tma_store_2d(os.map, b, x, y);
+    bulk_commit();
+  }
+  ++os.issued;
+}
+
 // Epilogue of one 256-column accumulator tile for this thread's row.
 //   tbase      TMEM address of (this warp's lane quarter, column 0 of the tile)
 //   row        kFwd/kDz/kDh: row within the chunk; kDw: vocabulary row
@@ -80,10 +120,12 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 //   have_acc   false only for kDw with an empty K range (writes zeros)
 //   split_idx, splits  kDh with its K range split: write fp32 partial sums
 //   release    called once, right after the last TMEM load of the tile
+//   os         the warp's output staging (kDz, kDw)
 template <int MODE, typename Release>
 __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tbase, int row,
                                               int nt, int cstart, int rows_valid, bool have_acc,
-                                              int split_idx, int splits, Release&& release) {
+                                              int split_idx, int splits, OutStage& os,
+                                              Release&& release) {
   constexpr int kSlices = kBN / 32;
   const int col_tile = nt * kBN;
 
@@ -172,7 +214,11 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
         cb = glp;
       }
     }
-    __nv_bfloat16* drow = p.dz + static_cast<int64_t>(row) * p.dz_ld;
+    // The warp's rows [row0, row0 + 32) of dZ leave in boxes of 64 columns:
+    // two 32-column slices fill one box (chunks 0-3, then 4-7).
+    const int lane = threadIdx.x & 31;
+    const int row0 = row - lane;
+    uint8_t* b = nullptr;
 #pragma unroll 1
     for (int c = 0; c < kSlices; ++c) {
       uint32_t r[32];
@@ -181,7 +227,8 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
       tmem_ld_wait();
       if (c == kSlices - 1) release();
       const int col = col_tile + c * 32;
-      if (col >= p.V) continue;
+      const int box_col = col_tile + (c & ~1) * 32;
+      if (box_col >= p.V) continue;  // warp-uniform: the box lies past the vocabulary
       uint32_t packed[16];
       if (row_ok) {
         float g[32];
@@ -202,12 +249,13 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
 #pragma unroll
         for (int j = 0; j < 16; ++j) packed[j] = 0u;
       }
-      uint4* dst = reinterpret_cast<uint4*>(drow + col);
+      if ((c & 1) == 0) b = out_buffer(os, lane);
 #pragma unroll
       for (int v = 0; v < 4; ++v)
-        if (col + 8 * v < p.V)
-          dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                              packed[4 * v + 3]);
+        out_put(b, lane, (c & 1) * 4 + v,
+                make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                           packed[4 * v + 3]));
+      if (c & 1) out_issue(os, b, lane, box_col, row0, false);
     }
   } else if (MODE == kDh) {
     const bool row_ok = row < rows_valid && (p.lvalid == nullptr || p.lvalid[cstart + row] != 0);
@@ -246,8 +294,11 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
       }
     }
   } else {  // kDw
-    const bool row_ok = row < p.V;
-    float* wrow = p.dw + static_cast<int64_t>(row_ok ? row : 0) * p.H;
+    // The warp's rows [row0, row0 + 32) of dW (vocabulary rows; rows past V
+    // are clipped by the map) leave in boxes of 32 fp32 columns, added to dW
+    // at L2 when accumulating, stored otherwise.
+    const int lane = threadIdx.x & 31;
+    const int row0 = row - lane;
 #pragma unroll 1
     for (int c = 0; c < kSlices; ++c) {
       uint32_t r[32];
@@ -261,20 +312,14 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
         for (int j = 0; j < 32; ++j) r[j] = 0u;
       }
       const int col = col_tile + c * 32;
-      if (!row_ok || col >= p.H) continue;
-      float4* dst = reinterpret_cast<float4*>(wrow + col);
+      // warp-uniform: no box starts past the matrix (rows past V inside a
+      // box are clipped by the map)
+      if (col >= p.H || row0 >= p.V) continue;
+      uint8_t* b = out_buffer(os, lane);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        if (col + 4 * v < p.H) {
-          float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          if (p.beta) {
-            const float4 old = dst[v];
-            o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-          }
-          dst[v] = o;
-        }
-      }
+      for (int v = 0; v < 8; ++v)
+        out_put(b, lane, v, make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]));
+      out_issue(os, b, lane, col, row0, p.beta != 0);
     }
   }
 }

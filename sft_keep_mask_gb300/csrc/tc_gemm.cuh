@@ -37,13 +37,15 @@ namespace lmhead {
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                   const __grid_constant__ CUtensorMap tma_b, const TcGemmParams p) {
+                   const __grid_constant__ CUtensorMap tma_b,
+                   const __grid_constant__ CUtensorMap tma_c, const TcGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint8_t* sOut = sB + kStages * kBBytes;  // kDz / kDw output staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + out_stage_bytes(MODE));
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -80,6 +82,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
+    if (out_stage_bytes(MODE) > 0) tma_prefetch_desc(&tma_c);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int row_local = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    OutStage os{&tma_c, sOut + (warp - 2) * 2 * kOutBoxBytes, 0u};
     int it = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
       const int t = u % num_tiles;
@@ -205,11 +209,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
       uint64_t* te = &tempty[acc];
-      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, cstart, rows_valid, num_kb > 0, sidx, splits, [&] {
+      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, cstart, rows_valid, num_kb > 0, sidx, splits, os, [&] {
         tc_fence_before();
         mbar_arrive(te);
       });
     }
+    // the output writes have finished before the CTA's shared memory goes
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -222,7 +229,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <int MODE>
 cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
-                           const TcGemmParams& p, int grid, cudaStream_t stream) {
+                           const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
+                           cudaStream_t stream) {
   // the shared-memory opt-in is per device: set it once on each device used
   static bool configured[64] = {};
   int dev = 0;
@@ -230,11 +238,13 @@ cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm_smem_bytes<MODE>());
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  tc_gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(tma_a, tma_b, p);
+  tc_gemm_kernel<MODE><<<grid, kGemmThreads, gemm_smem_bytes<MODE>(), stream>>>(tma_a, tma_b, tma_c,
+                                                                              p);
   return cudaGetLastError();
 }
 

@@ -26,19 +26,24 @@ namespace lmhead {
 constexpr int kPairStages = 6;
 constexpr int kPairABytes = 128 * kBK * 2;   // this CTA's half of A
 constexpr int kPairBBytes = 128 * kBK * 2;   // this CTA's half of B
-constexpr int kPairSmemBytes = kPairStages * (kPairABytes + kPairBBytes) + 1024 + 256;
+template <int MODE>
+constexpr int pair_smem_bytes() {
+  return kPairStages * (kPairABytes + kPairBBytes) + out_stage_bytes(MODE) + 1024 + 256;
+}
 constexpr int kPairTileM = 256;
 
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
-                        const __grid_constant__ CUtensorMap tma_b, const TcGemmParams p) {
+                        const __grid_constant__ CUtensorMap tma_b,
+                        const __grid_constant__ CUtensorMap tma_c, const TcGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kPairStages * kPairABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPairStages * kPairBBytes);
+  uint8_t* sOut = sB + kPairStages * kPairBBytes;  // kDz / kDw output staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + out_stage_bytes(MODE));
   uint64_t* empty = full + kPairStages;
   uint64_t* tfull = empty + kPairStages;
   uint64_t* tempty = tfull + 2;
@@ -79,6 +84,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
+    if (out_stage_bytes(MODE) > 0) tma_prefetch_desc(&tma_c);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -195,6 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int row_local = static_cast<int>(rank) * 128 + q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    OutStage os{&tma_c, sOut + (warp - 2) * 2 * kOutBoxBytes, 0u};
     int it = 0;
     for (int u = pair; u < num_units; u += num_pairs, ++it) {
       const int t = u % num_tiles;
@@ -210,12 +217,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
       const uint32_t te = map_to_cta(smem_addr(&tempty[acc]), 0);
       epilogue_tile<MODE>(p, tbase, mt * kPairTileM + row_local, nt, cstart, rows_valid, num_kb > 0, sidx, splits,
-                          [&] {
+                          os, [&] {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive_cluster(te);
                           });
     }
+    // the output writes have finished before the CTA's shared memory goes
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -228,7 +238,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
 template <int MODE>
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
-                                const TcGemmParams& p, int grid, cudaStream_t stream) {
+                                const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
+                                cudaStream_t stream) {
   // the shared-memory opt-in is per device: set it once on each device used
   static bool configured[64] = {};
   int dev = 0;
@@ -236,11 +247,13 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair_smem_bytes<MODE>());
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  tc_gemm_pair_kernel<MODE><<<grid, kGemmThreads, kPairSmemBytes, stream>>>(tma_a, tma_b, p);
+  tc_gemm_pair_kernel<MODE><<<grid, kGemmThreads, pair_smem_bytes<MODE>(), stream>>>(tma_a, tma_b,
+                                                                                   tma_c, p);
   return cudaGetLastError();
 }
 
