@@ -66,7 +66,7 @@ def recorded_traffic(kernel, config):
         return None
     if rec.get("source_sha256") != kernel_source_digest():
         return None
-    for key in ("workload", "N", "H", "V", "chunk_rows", "mode", "keep_mask"):
+    for key in ("workload", "N", "H", "V", "chunk_rows", "mode", "keep_mask", "rows", "entropy"):
         if rec.get("config", {}).get(key) != config.get(key):
             return None
     return rec.get("kernels", {}).get(kernel)
