@@ -12,9 +12,11 @@
 //   kDz   dz = g_lp (1[v=y] - p) - g_ent p (log p + H) from the recomputed
 //         logit, p = exp(z - lse) (the backward of the same page; logits
 //         recomputed rather than saved, twinkle pull request #283, section 1),
-//         stored as bf16.
-//   kDh   bf16 rows scattered to dhidden[idx[row]].
-//   kDw   fp32 dW tile, written or added to.
+//         rounded to bf16 and written by TMA stores from shared memory.
+//   kDh   bf16 rows scattered to dhidden[idx[row]] (fp32 partial rows when
+//         the K range is split).
+//   kDw   fp32 dW tile, written by TMA stores (first chunk) or added to dW by
+//         TMA reduce-adds at L2.
 #pragma once
 
 #include <cstdint>

@@ -11,7 +11,8 @@
 //               accumulators, so the epilogue of tile i overlaps the MMAs of
 //               tile i+1
 //   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. one
-//               accumulator row per thread, 32 columns per tcgen05.ld
+//               accumulator row per thread, 32 columns per tcgen05.ld; kDz /
+//               kDw stage their output in shared memory for TMA writes
 //
 // Operand majors per contraction (K-major = K contiguous in global memory):
 //   kFwd, kDz : A = Hc [rows, H] K-major,  B = W [V, H] K-major

@@ -5,14 +5,16 @@
 // stages its 128-row half of A and its 128-row half of B, the even CTA issues
 // the MMAs for both, and each CTA's tensor memory receives its 128 accumulator
 // rows (all 256 columns).  Per CTA a K step stages 32 KB instead of 48 KB, so
-// six stages fit and every operand byte fetched from L2 feeds twice the FLOPs.
+// six stages fit, and every operand byte fetched from L2 feeds 1.5 times the
+// FLOPs of the one-CTA tile.
 //
 //   warp 0      TMA producer of this CTA's halves; both CTAs count the bytes
 //               on the even CTA's full barrier
 //   warp 1      TMEM allocation (both CTAs, collectively) and, in the even
 //               CTA, the MMA issuer; commits are multicast to both CTAs
 //   warps 2..5  epilogue of this CTA's 128 rows; one elected lane per warp
-//               releases the accumulator on the even CTA's barrier
+//               releases the accumulator on the even CTA's barrier and, for
+//               kDz / kDw, issues the warp's TMA output writes
 #pragma once
 
 #include <cstdint>
