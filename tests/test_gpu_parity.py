@@ -438,3 +438,14 @@ def test_random_shape_sweep():
                       grad_entropy=ent)
         finally:
             del os.environ["LMHEAD_GEMM"]
+
+
+@pytest.mark.parametrize("variant", ["pair", "single"])
+def test_wide_hidden_and_long_vocabulary(monkeypatch, variant):
+    # H = 8192: 128 K steps in the projections and 32 column tiles in dHidden
+    # and dW; V = 200000: 782 vocabulary tiles ending in a 64-wide tail, so
+    # the last dZ box and the last dW rows reach past the matrix and are
+    # clipped by the output maps
+    monkeypatch.setenv("LMHEAD_GEMM", variant)
+    _run_both(synth.workload("tiny", seed=510, N=520, H=8192, V=3000), chunk_rows=256)
+    _run_both(synth.workload("tiny", seed=511, N=96, H=256, V=200000), chunk_rows=256)
