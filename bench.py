@@ -159,13 +159,45 @@ def _oracle_sample(inp, keep, rows, want_grad=True):
     return h, y, g1, g2
 
 
-def cpu_oracle_rate(inp, keep_np, W64, rows):
+def cpu_oracle_rate(inp, keep_np, W64, rows, mode="fwdbwd", entropy_grad=True):
+    """Oracle time for `rows` sampled kept rows: the forward, plus for
+    mode "fwdbwd" the dhidden and dW contributions (with the entropy term
+    when `entropy_grad`)."""
     from oracle import lmhead_oracle as O
     h, y, g1, g2 = _oracle_sample(inp, keep_np, rows)
+    if mode != "fwdbwd":
+        g1 = g2 = None
+    elif not entropy_grad:
+        g2 = None
     t0 = time.perf_counter()
     O.score_rows(h, W64, y, g1, g2)
     dt = time.perf_counter() - t0
     return rows / dt, dt
+
+
+L2_BYTES = 126.5e6
+
+
+def run_config(args, N, H, V, nk, world, entropy_grad):
+    """The `config` object of the JSON line (both arms)."""
+    w_bytes, h_bytes = V * H * 2, N * H * 2
+    big = w_bytes + h_bytes > L2_BYTES
+    return {"workload": args.workload, "N": N, "H": H, "V": V, "kept_rows": nk,
+            "kept_frac": nk / N if N else 0.0, "chunk_rows": args.chunk_rows or 8192,
+            "entropy": "differentiable" if entropy_grad else "metric-only",
+            "mode": args.mode, "keep_mask": "off" if args.keep_off else "on",
+            "rows": "block-sparse tiles" if args.blocksparse else "compacted",
+            "l2": ("inputs larger than L2" if big else "inputs fit in L2 (no flush)")
+                  + f" (W {w_bytes / 1e9:.2f} GB, hidden {h_bytes / 1e9:.2f} GB)",
+            "parallelism": f"replicas x{world}"}
+
+
+def entropy_grad_of(args, inp):
+    """Whether the step differentiates the entropy (the workload's default
+    unless --entropy-grad says otherwise)."""
+    if args.entropy_grad < 0:
+        return inp["grad_entropy"] is not None
+    return bool(args.entropy_grad) and inp["grad_entropy"] is not None
 
 
 def _workload(args):
@@ -213,31 +245,37 @@ def run_reference(args):
     from sft_keep_mask_gb300 import synth
     w = _workload(args)
     inp = synth.make_inputs(w, device="cpu")
-    keep = O.build_keep_mask([c.numpy() for c in inp["components"]], inp["seq_lens"]) \
-        if "components" in inp else inp["keep"].numpy()
+    if args.keep_off:
+        keep = np.ones(w.N, dtype=np.uint8)
+    elif "components" in inp:
+        keep = O.build_keep_mask([c.numpy() for c in inp["components"]], inp["seq_lens"])
+    else:
+        keep = inp["keep"].numpy()
     nk = int(keep.sum())
+    ent_grad = entropy_grad_of(args, inp)
     W64 = inp["weight"].float().double().numpy()
-    rows = args.ref_rows
+    rows = min(args.ref_rows, nk)
     for _ in range(args.warmup):
-        cpu_oracle_rate(inp, keep, W64, rows)
+        cpu_oracle_rate(inp, keep, W64, rows, args.mode, ent_grad)
     times = []
     for _ in range(args.steps):
-        _, dt = cpu_oracle_rate(inp, keep, W64, rows)
+        _, dt = cpu_oracle_rate(inp, keep, W64, rows, args.mode, ent_grad)
         times.append(dt)
     tot = sum(times)
     value = rows * args.steps / tot
-    flops = 8.0 * rows * w.H * w.V * args.steps
+    flops = (8.0 if args.mode == "fwdbwd" else 2.0) * rows * w.H * w.V * args.steps
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "N": w.N, "H": w.H, "V": w.V, "kept_rows": nk,
-                   "sample_rows_per_step": rows},
+        "config": dict(run_config(args, w.N, w.H, w.V, nk, world, ent_grad),
+                       sample_rows_per_step=rows),
         "tflops": flops / tot / 1e12,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
-                         "sample": f"{rows} kept rows per step, full H and V, forward + "
-                                   "dhidden + dW contribution, float64 numpy"},
+                         "sample": f"{rows} kept rows per step, full H and V, forward"
+                                   + (" + dhidden + dW contribution" if args.mode == "fwdbwd"
+                                      else "") + ", float64 numpy"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -279,8 +317,7 @@ def run_ours(args):
     dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
     dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     ws = sc.workspace
-    use_ent_grad = (inp["grad_entropy"] is not None) if args.entropy_grad < 0 else bool(
-        args.entropy_grad)
+    use_ent_grad = entropy_grad_of(args, inp)
     g_ent = inp["grad_entropy"] if use_ent_grad else None
     stream = torch.cuda.current_stream(dev)
 
@@ -394,12 +431,15 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import numpy as np
-        keep_np = keep.cpu().numpy()
+        # the keep-off arm scores every row (its keep buffer is never filled)
+        keep_np = np.ones(N, np.uint8) if args.keep_off else keep.cpu().numpy()
         W64 = inp["weight"].float().cpu().double().numpy()
-        rate, dt = cpu_oracle_rate(inp, keep_np, W64, args.ref_rows)
+        rows = min(args.ref_rows, nk)
+        rate, dt = cpu_oracle_rate(inp, keep_np, W64, rows, args.mode, g_ent is not None)
+        what = "forward + dhidden + dW contribution" if args.mode == "fwdbwd" else "forward"
         cpu = {"value": rate, "unit": UNIT, "cores": _cores(), "kind": "oracle",
-               "sample": f"{args.ref_rows} kept rows, full H and V: forward + dhidden + dW "
-                         f"contribution in float64 numpy ({dt:.1f} s)"}
+               "sample": f"{rows} kept rows, full H and V: {what} in float64 numpy "
+                         f"({dt:.1f} s)"}
 
     if rank == 0:
         line = {
@@ -407,13 +447,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": args.workload, "N": N, "H": H, "V": V, "kept_rows": nk,
-                       "kept_frac": nk / N, "chunk_rows": args.chunk_rows or 8192,
-                       "entropy": "differentiable" if g_ent is not None else "metric-only",
-                       "mode": args.mode, "keep_mask": "off" if args.keep_off else "on",
-                       "rows": "block-sparse tiles" if args.blocksparse else "compacted",
-                       "l2": "inputs larger than L2 (W 1.2 GB, hidden 0.5 GB)",
-                       "parallelism": f"replicas x{world}"},
+            "config": run_config(args, N, H, V, nk, world, g_ent is not None),
             "peak_device_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
             "logits_bf16_gb_avoided": N * V * 2 / 1e9,
             "tflops": tflops, "frac_of_peak": tflops / burst,

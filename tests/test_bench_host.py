@@ -29,3 +29,26 @@ def test_traffic_record_is_dropped_when_the_sources_change(monkeypatch):
     rec = _record()
     monkeypatch.setattr(bench, "kernel_source_digest", lambda: "0" * 64)
     assert bench.recorded_traffic("gemm_dw", dict(rec["config"])) is None
+
+
+def test_reference_arm_prints_the_contract_line():
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == line["value"] and cpu["cores"] >= 1
+    # the same config object as the GPU arm (plus the size of the sample)
+    import argparse
+    args = argparse.Namespace(workload="tiny", chunk_rows=0, mode="fwdbwd", keep_off=False,
+                              blocksparse=False)
+    cfg = line["config"]
+    want = bench.run_config(args, cfg["N"], cfg["H"], cfg["V"], cfg["kept_rows"], 1, True)
+    assert {k: cfg[k] for k in want} == want
+    assert cfg["sample_rows_per_step"] == cfg["kept_rows"]  # tiny: fewer kept rows than 256
