@@ -95,9 +95,35 @@ def _p(t):
     return None if t is None else _VP(t.data_ptr())
 
 
-def _s(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _s(stream, device=None):
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return _VP(s.cuda_stream)
+
+
+def _device_of(*tensors):
+    """The one CUDA device of the given tensors (None ignored); the library
+    launches on the current device, so every call runs under this one."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise TypeError("every tensor argument must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors on different devices ({dev} and {t.device})")
+    return dev
+
+
+def _call(name, tensors, *args, stream=None):
+    """Runs lib().<name>(*args, stream) on the tensors' device and returns the
+    status code."""
+    dev = _device_of(*tensors)
+    if dev is None:
+        return getattr(lib(), name)(*args, _s(stream))
+    with torch.cuda.device(dev):
+        return getattr(lib(), name)(*args, _s(stream, dev))
 
 
 def _check(code, where):
@@ -133,9 +159,9 @@ def lmhead_build_keep_mask(loss_mask, ce_weight, kl_weight, seq_offsets, keep, s
         _need(t, torch.float32, name, N)
     _need(seq_offsets, torch.int32, "seq_offsets")
     _need(keep, torch.uint8, "keep")
-    code = lib().lmhead_build_keep_mask(_p(loss_mask), _p(ce_weight), _p(kl_weight),
-                                        _p(seq_offsets), seq_offsets.numel() - 1, N, _p(keep),
-                                        _s(stream))
+    code = _call("lmhead_build_keep_mask", (loss_mask, ce_weight, kl_weight, seq_offsets, keep),
+                 _p(loss_mask), _p(ce_weight), _p(kl_weight), _p(seq_offsets),
+                 seq_offsets.numel() - 1, N, _p(keep), stream=stream)
     _check(code, "lmhead_build_keep_mask")
 
 
@@ -147,8 +173,9 @@ def lmhead_compact(keep, targets, V, idx, targets_c, d_nk, workspace, stream=Non
     _need(targets_c, torch.int32, "targets_c", N)
     _need(d_nk, torch.int32, "d_nk", 1)
     _need(workspace, torch.uint8, "workspace")
-    code = lib().lmhead_compact(_p(keep), _p(targets), N, V, _p(idx), _p(targets_c), _p(d_nk),
-                                _p(workspace), workspace.numel(), _s(stream))
+    code = _call("lmhead_compact", (keep, targets, idx, targets_c, d_nk, workspace),
+                 _p(keep), _p(targets), N, V, _p(idx), _p(targets_c), _p(d_nk), _p(workspace),
+                 workspace.numel(), stream=stream)
     _check(code, "lmhead_compact")
 
 
@@ -164,9 +191,10 @@ def lmhead_fwd(hidden, weight, targets, keep, want_entropy, logprob, entropy, ls
     _need(entropy, torch.float32, "entropy", N)
     _need(lse, torch.float32, "lse", N)
     _need(workspace, torch.uint8, "workspace")
-    code = getattr(lib(), _entry)(_p(hidden), _p(weight), _p(targets), _p(keep), N, H, V,
-                                  int(bool(want_entropy)), _p(logprob), _p(entropy), _p(lse),
-                                  int(chunk_rows), _p(workspace), workspace.numel(), _s(stream))
+    code = _call(_entry, (hidden, weight, targets, keep, logprob, entropy, lse, workspace),
+                 _p(hidden), _p(weight), _p(targets), _p(keep), N, H, V,
+                 int(bool(want_entropy)), _p(logprob), _p(entropy), _p(lse), int(chunk_rows),
+                 _p(workspace), workspace.numel(), stream=stream)
     _check(code, _entry)
 
 
@@ -185,10 +213,12 @@ def lmhead_bwd(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_e
     _need(dhidden, torch.bfloat16, "dhidden", N * H)
     _need(dweight, torch.float32, "dweight", V * H)
     _need(workspace, torch.uint8, "workspace")
-    code = getattr(lib(), _entry)(_p(hidden), _p(weight), _p(targets), _p(keep), N, H, V,
-                                  _p(lse), _p(entropy), _p(grad_logprob), _p(grad_entropy),
-                                  _p(dhidden), _p(dweight), int(bool(dw_accumulate)),
-                                  int(chunk_rows), _p(workspace), workspace.numel(), _s(stream))
+    code = _call(_entry, (hidden, weight, targets, keep, lse, entropy, grad_logprob,
+                          grad_entropy, dhidden, dweight, workspace),
+                 _p(hidden), _p(weight), _p(targets), _p(keep), N, H, V, _p(lse), _p(entropy),
+                 _p(grad_logprob), _p(grad_entropy), _p(dhidden), _p(dweight),
+                 int(bool(dw_accumulate)), int(chunk_rows), _p(workspace), workspace.numel(),
+                 stream=stream)
     _check(code, _entry)
 
 
@@ -216,10 +246,10 @@ def lmhead_fwd_shard(hidden, weight_shard, v_begin, V_total, targets, keep, want
     _need(keep, torch.uint8, "keep", N)
     _need(partials, torch.float32, "partials", N * 4)
     _need(workspace, torch.uint8, "workspace")
-    code = lib().lmhead_fwd_shard(_p(hidden), _p(weight_shard), _p(targets), _p(keep), N, H, Vs,
-                                  int(v_begin), int(V_total), int(bool(want_entropy)),
-                                  _p(partials), int(chunk_rows), _p(workspace),
-                                  workspace.numel(), _s(stream))
+    code = _call("lmhead_fwd_shard", (hidden, weight_shard, targets, keep, partials, workspace),
+                 _p(hidden), _p(weight_shard), _p(targets), _p(keep), N, H, Vs, int(v_begin),
+                 int(V_total), int(bool(want_entropy)), _p(partials), int(chunk_rows),
+                 _p(workspace), workspace.numel(), stream=stream)
     _check(code, "lmhead_fwd_shard")
 
 
@@ -230,8 +260,9 @@ def lmhead_merge_shards(partials, keep, want_entropy, logprob, entropy, lse, str
     _need(logprob, torch.float32, "logprob", N)
     _need(entropy, torch.float32, "entropy", N)
     _need(lse, torch.float32, "lse", N)
-    code = lib().lmhead_merge_shards(_p(partials), S, _p(keep), N, int(bool(want_entropy)),
-                                     _p(logprob), _p(entropy), _p(lse), _s(stream))
+    code = _call("lmhead_merge_shards", (partials, keep, logprob, entropy, lse),
+                 _p(partials), S, _p(keep), N, int(bool(want_entropy)), _p(logprob),
+                 _p(entropy), _p(lse), stream=stream)
     _check(code, "lmhead_merge_shards")
 
 
@@ -251,11 +282,13 @@ def lmhead_bwd_shard(hidden, weight_shard, v_begin, V_total, targets, keep, lse,
     _need(dhidden_partial, torch.bfloat16, "dhidden_partial", N * H)
     _need(dweight_shard, torch.float32, "dweight_shard", Vs * H)
     _need(workspace, torch.uint8, "workspace")
-    code = lib().lmhead_bwd_shard(_p(hidden), _p(weight_shard), _p(targets), _p(keep), N, H, Vs,
-                                  int(v_begin), int(V_total), _p(lse), _p(entropy),
-                                  _p(grad_logprob), _p(grad_entropy), _p(dhidden_partial),
-                                  _p(dweight_shard), int(bool(dw_accumulate)), int(chunk_rows),
-                                  _p(workspace), workspace.numel(), _s(stream))
+    code = _call("lmhead_bwd_shard", (hidden, weight_shard, targets, keep, lse, entropy,
+                                       grad_logprob, grad_entropy, dhidden_partial,
+                                       dweight_shard, workspace),
+                 _p(hidden), _p(weight_shard), _p(targets), _p(keep), N, H, Vs, int(v_begin),
+                 int(V_total), _p(lse), _p(entropy), _p(grad_logprob), _p(grad_entropy),
+                 _p(dhidden_partial), _p(dweight_shard), int(bool(dw_accumulate)),
+                 int(chunk_rows), _p(workspace), workspace.numel(), stream=stream)
     _check(code, "lmhead_bwd_shard")
 
 
@@ -264,7 +297,8 @@ def lmhead_expand(src, idx, d_nk, N, dst, stream=None):
     _need(idx, torch.int32, "idx")
     _need(d_nk, torch.int32, "d_nk", 1)
     _need(dst, torch.float32, "dst", N)
-    code = lib().lmhead_expand(_p(src), _p(idx), _p(d_nk), N, _p(dst), _s(stream))
+    code = _call("lmhead_expand", (src, idx, d_nk, dst), _p(src), _p(idx), _p(d_nk), N, _p(dst),
+                 stream=stream)
     _check(code, "lmhead_expand")
 
 
@@ -292,9 +326,11 @@ def lmhead_selective_log_softmax_fwd(logits, targets, keep, want_entropy, logpro
     _need(entropy, torch.float32, "entropy", N)
     _need(lse, torch.float32, "lse", N)
     _need(d_status, torch.int32, "d_status", 1)
-    code = lib().lmhead_selective_log_softmax_fwd(
-        _p(logits), _logits_dtype(logits), ld, _p(targets), _p(keep), N, V,
-        int(bool(want_entropy)), _p(logprob), _p(entropy), _p(lse), _p(d_status), _s(stream))
+    code = _call("lmhead_selective_log_softmax_fwd",
+                 (logits, targets, keep, logprob, entropy, lse, d_status),
+                 _p(logits), _logits_dtype(logits), ld, _p(targets), _p(keep), N, V,
+                 int(bool(want_entropy)), _p(logprob), _p(entropy), _p(lse), _p(d_status),
+                 stream=stream)
     _check(code, "lmhead_selective_log_softmax_fwd")
 
 
@@ -312,15 +348,18 @@ def lmhead_selective_log_softmax_bwd(logits, targets, keep, lse, entropy, grad_l
     _need(grad_logprob, torch.float32, "grad_logprob", N)
     _need(grad_entropy, torch.float32, "grad_entropy", N)
     _need(d_status, torch.int32, "d_status", 1)
-    code = lib().lmhead_selective_log_softmax_bwd(
-        _p(logits), _logits_dtype(logits), ld, _p(targets), _p(keep), N, V, _p(lse), _p(entropy),
-        _p(grad_logprob), _p(grad_entropy), _p(dlogits), ld_out, _p(d_status), _s(stream))
+    code = _call("lmhead_selective_log_softmax_bwd",
+                 (logits, targets, keep, lse, entropy, grad_logprob, grad_entropy, dlogits,
+                  d_status),
+                 _p(logits), _logits_dtype(logits), ld, _p(targets), _p(keep), N, V, _p(lse),
+                 _p(entropy), _p(grad_logprob), _p(grad_entropy), _p(dlogits), ld_out,
+                 _p(d_status), stream=stream)
     _check(code, "lmhead_selective_log_softmax_bwd")
 
 
 def lmhead_get_status(workspace, stream=None) -> int:
     """Device status of the last call on this workspace (synchronises)."""
-    return int(lib().lmhead_get_status(_p(workspace), _s(stream)))
+    return int(_call("lmhead_get_status", (workspace,), _p(workspace), stream=stream))
 
 
 def lmhead_workspace_kept_rows(workspace):

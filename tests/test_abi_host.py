@@ -134,3 +134,11 @@ def test_autograd_op_rejects_bad_arguments_before_any_call():
         hidden_to_logprobs(h, W, y, main_grad=torch.zeros(16, 8, dtype=torch.bfloat16))
     with pytest.raises(TypeError, match="main_grad"):
         hidden_to_logprobs(h, W, y, main_grad=torch.zeros(8, 16))
+
+
+def test_binding_runs_each_call_on_its_tensors_device():
+    import torch
+    from sft_keep_mask_gb300 import lmhead
+    assert lmhead._device_of(None, None) is None
+    with pytest.raises(TypeError, match="CUDA"):
+        lmhead._device_of(torch.zeros(2))  # host tensors never reach the library
