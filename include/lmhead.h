@@ -36,6 +36,9 @@
  *   - All array pointers are DEVICE pointers on the current CUDA device,
  *     allocated and owned by the caller.  The library never allocates device
  *     memory (the caller passes a workspace) and keeps no per-call state.
+ *     A pointer that is neither device memory of the current device nor
+ *     managed memory (a host pointer, another GPU's memory) is refused with
+ *     LMHEAD_EINVAL before anything is launched.
  *   - Matrices are row-major and contiguous.  hidden, weight (and dhidden)
  *     must be 16-byte aligned; H must be a multiple of 8.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
@@ -46,7 +49,9 @@
  *   - No C++ exception crosses this boundary and the library never exits the
  *     process.
  *   - Outputs are float32 (logprob, entropy, lse, dW) and bf16 (dhidden).
- *     Results are deterministic: no floating-point atomics are used.
+ *     Results are deterministic: each output element is written once per
+ *     launch, and dW's accumulation over chunks adds each element once per
+ *     chunk (a TMA reduce-add at L2), chunk after chunk in a fixed order.
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H
@@ -60,7 +65,8 @@ extern "C" {
 
 typedef enum {
   LMHEAD_OK = 0,
-  LMHEAD_EINVAL = 1,       /* bad argument: NULL pointer, size, alignment     */
+  LMHEAD_EINVAL = 1,       /* bad argument: NULL / non-device pointer, size,
+                              alignment                                       */
   LMHEAD_EWORKSPACE = 2,   /* workspace smaller than lmhead_workspace_size()   */
   LMHEAD_ETARGET = 3,      /* (device) a kept row's target is outside [0, V)   */
   LMHEAD_ECUDA = 4,        /* a CUDA runtime call failed                       */

@@ -81,6 +81,7 @@ extern "C" lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
       major != 10 || minor != 3)
     return LMHEAD_EUNSUPPORTED;
+  if (!device_ptrs_ok({keep, targets, idx, targets_c, d_nk, d_status})) return LMHEAD_EINVAL;
   int32_t* counts = nullptr;
   lmhead_status st = scratch_for_current_device(&counts);
   if (st != LMHEAD_OK) return st;

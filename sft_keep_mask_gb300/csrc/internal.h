@@ -2,11 +2,32 @@
 #pragma once
 
 #include <cstdint>
+#include <initializer_list>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace lmhead {
+
+// True when every non-null pointer is device memory of the current device
+// (or managed memory).  A host pointer or another GPU's memory passed as a
+// kernel buffer would make the kernels fault; the entry points refuse it
+// with LMHEAD_EINVAL instead.
+inline bool device_ptrs_ok(std::initializer_list<const void*> ptrs) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  for (const void* ptr : ptrs) {
+    if (ptr == nullptr) continue;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+      cudaGetLastError();  // not a sticky error: clear it
+      return false;
+    }
+    if (a.type == cudaMemoryTypeManaged) continue;
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return false;
+  }
+  return true;
+}
 
 // Tile shape of the tcgen05 GEMM: 128 x 256 fp32 accumulator in TMEM,
 // 64-element (128-byte) K steps staged by TMA with the 128-byte swizzle.

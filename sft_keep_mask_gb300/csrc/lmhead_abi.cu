@@ -239,6 +239,11 @@ DevInfo device_info() {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+#define LM_CHECK_PTRS(...)                                \
+  do {                                                    \
+    if (!device_ptrs_ok({__VA_ARGS__})) return LMHEAD_EINVAL; \
+  } while (0)
+
 lmhead_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LMHEAD_OK : LMHEAD_ECUDA; }
 
 #define LM_TRY(expr)                                  \
@@ -330,6 +335,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   if (st != LMHEAD_OK) return st;
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(hidden, weight, targets, keep, logprob, entropy, lse, partial, workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Range range("lmhead_fwd");
 
@@ -435,6 +441,8 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   st = check_ws(workspace, ws_bytes, L);
   if (st != LMHEAD_OK) return st;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(hidden, weight, targets, keep, lse, entropy, grad_logprob, grad_entropy, dhidden,
+                dweight, workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Range range("lmhead_bwd");
   if (N == 0) {
@@ -578,6 +586,7 @@ lmhead_status lmhead_build_keep_mask(const float* loss_mask, const float* ce_wei
   if (N < 0 || n_seq < 0 || seq_offsets == nullptr || keep == nullptr) return LMHEAD_EINVAL;
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(loss_mask, ce_weight, kl_weight, seq_offsets, keep);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Launch l(kKindBuildKeep, s);
   return cuda_status(launch_build_keep(loss_mask, ce_weight, kl_weight, seq_offsets, n_seq, N,
@@ -596,6 +605,7 @@ lmhead_status lmhead_compact(const uint8_t* keep, const int64_t* targets, int64_
     return LMHEAD_EINVAL;
   if (ws_bytes < need) return LMHEAD_EWORKSPACE;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(keep, targets, idx, targets_c, d_nk, workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = at<int>(workspace, L.hdr);
   LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
@@ -664,6 +674,7 @@ lmhead_status lmhead_merge_shards(const float* partials, int num_shards, const u
     return LMHEAD_EINVAL;
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(partials, keep, logprob, entropy, lse);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Launch l(kKindMergeShards, s);
   return cuda_status(launch_merge_shards(reinterpret_cast<const float4*>(partials), num_shards,
@@ -690,6 +701,7 @@ lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t*
     return LMHEAD_EINVAL;
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(src, idx, d_nk, dst);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Launch l(kKindExpand, s);
   return cuda_status(launch_expand(src, idx, d_nk, N, dst, s));
@@ -707,6 +719,7 @@ lmhead_status lmhead_selective_log_softmax_fwd(const void* logits, int logits_dt
     return LMHEAD_EINVAL;
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(logits, targets, keep, logprob, entropy, lse, d_status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Range range("lmhead_selective_log_softmax_fwd");
   Launch l(kKindSlsFwd, s);
@@ -730,6 +743,8 @@ lmhead_status lmhead_selective_log_softmax_bwd(const void* logits, int logits_dt
     return LMHEAD_EINVAL;
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
+  LM_CHECK_PTRS(logits, targets, keep, lse, entropy, grad_logprob, grad_entropy, dlogits,
+                d_status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Range range("lmhead_selective_log_softmax_bwd");
   Launch l(kKindSlsBwd, s);

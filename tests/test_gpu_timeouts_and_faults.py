@@ -94,3 +94,23 @@ def test_guard_bands_around_workspace_and_outputs():
         head = buf[:G].cpu().numpy()
         tail = buf[-G:].cpu().numpy()
         assert (head == 0xA5).all() and (tail == 0xA5).all(), f"{name} guard band overwritten"
+
+
+def test_host_memory_passed_as_a_device_buffer_is_refused():
+    # a pinned host buffer where device memory is expected: the call returns
+    # LMHEAD_EINVAL from its pointer check and launches nothing
+    w, inp = _small()
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    lib = L.lib()
+    out = [torch.empty(w.N, dtype=torch.float32, device=DEV) for _ in range(3)]
+    host_keep = inp["keep"].cpu().pin_memory()
+    stream = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    before = L.lmhead_launch_count()
+    code = lib.lmhead_fwd(inp["hidden"].data_ptr(), inp["weight"].data_ptr(),
+                          inp["targets"].data_ptr(), host_keep.data_ptr(), w.N, w.H, w.V, 1,
+                          out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(), 0,
+                          sc.workspace.data_ptr(), sc.workspace.numel(), stream)
+    assert code == L.LMHEAD_EINVAL
+    assert L.lmhead_launch_count() == before
+    _check_forward(w, inp, sc)  # the next valid call works
