@@ -19,6 +19,10 @@ the fp32 gradient is cast to the weight's dtype by torch for autograd.
 Everything else is argument marshalling; no step of the scoring runs outside
 the library.  Device-side errors (a kept row whose target is outside
 [0, V)) are reported through ``workspace_status``.
+
+Calls for the same head (device, H, V, chunk_rows) share one workspace, so
+they must be ordered on one stream (as forward and backward of a training
+step are); work on other streams needs its own ``LMHeadScorer``.
 """
 
 from __future__ import annotations
@@ -31,13 +35,26 @@ _workspaces: dict = {}
 
 
 def workspace_for(N: int, H: int, V: int, chunk_rows: int, device) -> torch.Tensor:
-    """The cached workspace of this shape on `device` (one per shape)."""
+    """A workspace for N rows of this head on `device`.
+
+    One buffer is kept per (device, H, V, chunk_rows) and reused for any N
+    whose workspace fits in it (the library lays the workspace out from N and
+    only needs enough bytes), so a batch size that changes from step to step
+    does not allocate a new workspace each time; it grows by a quarter beyond
+    the largest size asked for so far when it is too small.
+    """
     dev = torch.device(device)
-    key = (dev.type, dev.index, N, H, V, chunk_rows)
+    if dev.index is None:
+        dev = torch.device(dev.type, torch.cuda.current_device())
+    key = (dev.type, dev.index, H, V, chunk_rows)
+    need = max(L.lmhead_workspace_size(N, H, V, True, chunk_rows), 256)
     ws = _workspaces.get(key)
-    if ws is None:
-        nbytes = L.lmhead_workspace_size(N, H, V, True, chunk_rows)
-        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    if ws is None or ws.numel() < need:
+        if ws is not None:
+            need += need // 4
+            del _workspaces[key]
+            ws = None
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
         _workspaces[key] = ws
     return ws
 

@@ -107,3 +107,27 @@ def test_bad_target_on_a_kept_row_is_reported():
     h, W = _leaves(inp)
     hidden_to_logprobs(h, W, y, inp["keep"])
     assert workspace_status(h, W) == L.LMHEAD_ETARGET
+
+
+def test_changing_batch_size_reuses_one_workspace():
+    # RL batches change N from step to step: the op keeps one workspace per
+    # (device, H, V, chunk) and grows it only when a larger N needs more
+    from sft_keep_mask_gb300 import autograd as A
+    H, V = 128, 2100
+    sizes = []
+    for i, N in enumerate((700, 300, 650, 900, 500)):
+        w, inp = _inputs(seed=310 + i, N=N, H=H, V=V)
+        h, W = _leaves(inp)
+        lp = hidden_to_logprobs(h, W, inp["targets"], inp["keep"], chunk_rows=256)
+        (inp["grad_logprob"] * lp).sum().backward()
+        keep = inp["keep"].cpu().numpy()
+        y = inp["targets"].cpu().numpy()
+        odh, odW = O.backward(to64(h), to64(W), y, keep, to64(inp["grad_logprob"]))
+        assert_frob_close(to64(h.grad), odh, "dhidden")
+        assert_frob_close(to64(W.grad), odW, "dW")
+        ws = A.workspace_for(N, H, V, 256, h.device)
+        sizes.append(ws.numel())
+    keys = [k for k in A._workspaces if k[2:] == (H, V, 256)]
+    assert len(keys) == 1
+    # grew only for the two sizes larger than every earlier one
+    assert len(set(sizes)) <= 2
