@@ -12,7 +12,14 @@ from . import lmhead as L
 
 
 class LMHeadScorer:
-    """Fused LM-head scoring for fixed (N, H, V, chunk_rows)."""
+    """Fused LM-head scoring for one head (H, V, chunk_rows) and batches of up
+    to N rows.
+
+    The workspace is sized for N rows and serves any batch of at most N rows
+    (the library lays it out from each call's row count, and a smaller batch
+    needs no more bytes), so batch sizes that change from step to step reuse
+    it; outputs are sized by each call's batch.
+    """
 
     def __init__(self, N: int, H: int, V: int, chunk_rows: int = 0, device="cuda",
                  blocksparse: bool = False):
@@ -25,31 +32,40 @@ class LMHeadScorer:
         nbytes = L.lmhead_workspace_size(N, H, V, True, chunk_rows)
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
 
+    def _rows(self, n: int) -> int:
+        if n > self.N:
+            raise ValueError(f"batch of {n} rows exceeds this scorer's capacity of {self.N}")
+        return n
+
     def keep_mask(self, loss_mask=None, ce_weight=None, kl_weight=None, seq_lens=None,
                   stream=None):
         """Keep mask after the next-token shift from token-aligned loss components."""
+        comps = [c for c in (loss_mask, ce_weight, kl_weight) if c is not None]
+        n = self._rows(comps[0].numel() if comps else self.N)
         lens = torch.as_tensor(seq_lens, dtype=torch.int64)
         offsets = torch.zeros(lens.numel() + 1, dtype=torch.int32)
         offsets[1:] = torch.cumsum(lens, 0).to(torch.int32)
         offsets = offsets.to(self.device)
-        keep = torch.empty(self.N, dtype=torch.uint8, device=self.device)
+        keep = torch.empty(n, dtype=torch.uint8, device=self.device)
         L.lmhead_build_keep_mask(loss_mask, ce_weight, kl_weight, offsets, keep, stream)
         return keep
 
     def compact(self, keep, targets, stream=None):
-        idx = torch.empty(self.N, dtype=torch.int32, device=self.device)
-        yc = torch.empty(self.N, dtype=torch.int32, device=self.device)
+        n = self._rows(targets.numel())
+        idx = torch.empty(n, dtype=torch.int32, device=self.device)
+        yc = torch.empty(n, dtype=torch.int32, device=self.device)
         nk = torch.empty(1, dtype=torch.int32, device=self.device)
         L.lmhead_compact(keep, targets, self.V, idx, yc, nk, self.workspace, stream)
         return idx, yc, nk
 
     def forward(self, hidden, weight, targets, keep=None, want_entropy=True, stream=None,
                 out=None):
+        n = self._rows(hidden.shape[0])
         if out is None:
-            out = (torch.empty(self.N, dtype=torch.float32, device=self.device),
-                   torch.empty(self.N, dtype=torch.float32, device=self.device)
+            out = (torch.empty(n, dtype=torch.float32, device=self.device),
+                   torch.empty(n, dtype=torch.float32, device=self.device)
                    if want_entropy else None,
-                   torch.empty(self.N, dtype=torch.float32, device=self.device))
+                   torch.empty(n, dtype=torch.float32, device=self.device))
         lp, ent, lse = out
         fwd = L.lmhead_fwd_blocksparse if self.blocksparse else L.lmhead_fwd
         fwd(hidden, weight, targets, keep, want_entropy, lp, ent, lse, self.workspace,
@@ -58,6 +74,7 @@ class LMHeadScorer:
 
     def backward(self, hidden, weight, targets, keep, lse, entropy, grad_logprob,
                  grad_entropy=None, dweight=None, accumulate=False, stream=None, dhidden=None):
+        self._rows(hidden.shape[0])
         if dhidden is None:
             dhidden = torch.empty_like(hidden)
         if dweight is None:

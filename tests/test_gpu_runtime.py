@@ -150,3 +150,23 @@ def test_side_streams_and_two_concurrent_scorers_match_sequential_runs():
     for name, r, g in zip([f"a.{n}" for n in names] + [f"b.{n}" for n in names],
                           list(ref_a) + list(ref_b), list(got_a) + list(got_b)):
         assert torch.equal(r, g), name
+
+
+def test_one_scorer_serves_smaller_batches():
+    # the workspace of an N-row scorer serves any batch of at most N rows; the
+    # results equal those of a scorer sized for the batch, bit for bit
+    big = LMHeadScorer(1000, 192, 3000, chunk_rows=256)
+    for n, seed in ((600, 150), (1000, 151), (37, 152)):
+        w = synth.workload("tiny", seed=seed, N=n, H=192, V=3000)
+        inp = synth.make_inputs(w, device=DEV)
+        exact = LMHeadScorer(n, 192, 3000, chunk_rows=256)
+        got = _step_outputs(big, inp)
+        want = _step_outputs(exact, inp)
+        torch.cuda.synchronize()
+        assert big.status() == 0
+        for g, r in zip(got, want):
+            assert g.shape == r.shape and torch.equal(g, r)
+    w = synth.workload("tiny", seed=153, N=1001, H=192, V=3000)
+    inp = synth.make_inputs(w, device=DEV)
+    with pytest.raises(ValueError, match="capacity"):
+        big.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
