@@ -71,7 +71,10 @@ typedef enum {
   LMHEAD_ETARGET = 3,      /* (device) a kept row's target is outside [0, V)   */
   LMHEAD_ECUDA = 4,        /* a CUDA runtime call failed                       */
   LMHEAD_ETIMEOUT = 5,     /* (device) a pipeline wait gave up; results invalid*/
-  LMHEAD_EUNSUPPORTED = 6  /* the current device is not an sm_103 GPU          */
+  LMHEAD_EUNSUPPORTED = 6, /* the current device is not an sm_103 GPU          */
+  LMHEAD_EBOUNDS = 7       /* (device) an index outside its array was skipped:
+                              a caller's index (lmhead_expand), or in the
+                              LMHEAD_DEBUG build any checked internal index  */
 } lmhead_status;
 
 /* Opaque cudaStream_t. */
@@ -261,9 +264,13 @@ lmhead_status lmhead_bwd_shard(const void* hidden, const void* weight_shard,
  *   src  : float32 [Nk]   idx : int32 [Nk] (from lmhead_compact)
  *   d_nk : int32 [1] on the device (from lmhead_compact)
  *   dst (out) : float32 [N]; dst[idx[k]] = src[k], +0.0 elsewhere.
+ *   d_status (out, nullable) : int32 [1] on the device.  idx and d_nk come
+ *            from the caller: an entry of idx outside [0, N), or Nk > N, is
+ *            skipped (nothing is written for it) and sets *d_status to
+ *            LMHEAD_EBOUNDS (the caller clears it).
  */
 lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t* d_nk,
-                            int64_t N, float* dst, lmhead_stream_t stream);
+                            int64_t N, float* dst, int32_t* d_status, lmhead_stream_t stream);
 
 /* Element types of a logit matrix. */
 #define LMHEAD_DTYPE_BF16 0

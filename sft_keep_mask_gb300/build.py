@@ -19,6 +19,10 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "liblmhead.so")
+# The same sources with -DLMHEAD_DEBUG: device-side index checks that report
+# LMHEAD_EBOUNDS instead of touching memory outside an array.
+DEBUG_BUILD = os.path.join(PKG, "_build_debug")
+DEBUG_LIB = os.path.join(LIBDIR, "liblmhead_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -41,17 +45,22 @@ def _deps():
         os.path.join(ROOT, "include", "lmhead.h")]
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if stale) and return the path of the shared library."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile (if stale) and return the path of the shared library; with
+    `debug` the LMHEAD_DEBUG variant (liblmhead_debug.so)."""
+    build_dir = DEBUG_BUILD if debug else BUILD
+    lib_path = DEBUG_LIB if debug else LIB
+    if debug:
+        extra_flags = list(extra_flags) + ["-DLMHEAD_DEBUG"]
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     nvcc = _nvcc()
     newest_dep = max(os.path.getmtime(p) for p in _deps())
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest_dep:
-        return LIB
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= newest_dep:
+        return lib_path
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src[:-3] + ".o")
+        obj = os.path.join(build_dir, src[:-3] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,13 +72,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 EXAMPLE_SRC = os.path.join(PKG, "examples", "lmhead_c_example.c")
@@ -93,4 +102,5 @@ def build_example() -> str:
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else []))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else [],
+                debug="--debug" in sys.argv))

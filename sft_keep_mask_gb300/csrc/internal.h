@@ -29,6 +29,21 @@ inline bool device_ptrs_ok(std::initializer_list<const void*> ptrs) {
   return true;
 }
 
+// Debug builds (-DLMHEAD_DEBUG): every index the kernels derive from data is
+// checked before the access it guards; a failed check records LMHEAD_EBOUNDS
+// (7) in the status word and the access is skipped.  This stands in for a
+// memory checker that cannot run here.  Release builds compile the checks
+// out (LM_DCHECK is then the constant true).
+#ifdef LMHEAD_DEBUG
+__device__ __forceinline__ bool lm_index_ok(bool ok, int* status) {
+  if (!ok && status != nullptr) atomicCAS(status, 0, 7);
+  return ok;
+}
+#define LM_DCHECK(cond, status) lm_index_ok((cond), (status))
+#else
+#define LM_DCHECK(cond, status) true
+#endif
+
 // Tile shape of the tcgen05 GEMM: 128 x 256 fp32 accumulator in TMEM,
 // 64-element (128-byte) K steps staged by TMA with the 128-byte swizzle.
 constexpr int kBM = 128;
@@ -66,6 +81,7 @@ struct TcGemmParams {
   int H;
   int group_m;              // M tiles per raster block, 0 = none (see tile_coords)
   int group_n;              // N tiles per raster group when group_m == 0
+  int64_t n_rows;           // N, rows of the batch (index checks of debug builds)
   int* status;              // device status word
   // epilogue operands (compact, indexed by compact row)
   const int32_t* targets_c;
@@ -181,9 +197,10 @@ cudaError_t launch_tile_scan(const uint8_t* keep, const int64_t* targets, int64_
                              int32_t* tile_list, int32_t* d_na, int32_t* counts, int32_t* idx,
                              int32_t* targets_c, uint8_t* lvalid, int32_t* d_nk, int* status,
                              cudaStream_t s);
+// (N and status serve the index checks of debug builds.)
 cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
                                const int32_t* d_nk, int chunk_index, int chunk_rows, int H,
-                               __nv_bfloat16* hc, cudaStream_t s);
+                               __nv_bfloat16* hc, int64_t N, int* status, cudaStream_t s);
 cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
                          float* lse_c, float4* raw_c, cudaStream_t s);
@@ -191,21 +208,24 @@ cudaError_t launch_merge_shards(const float4* partials, int num_shards, const ui
                                 int64_t N, int want_entropy, float* lp, float* ent, float* lse,
                                 cudaStream_t s);
 cudaError_t launch_expand4(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk, int64_t N,
-                           const float4* src, float4* dst, cudaStream_t s);
+                           const float4* src, float4* dst, int* status, cudaStream_t s);
 cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,
                            int64_t N, const float* a_c, const float* b_c, const float* c_c,
-                           float* a, float* b, float* c, const uint8_t* lvalid, cudaStream_t s);
+                           float* a, float* b, float* c, const uint8_t* lvalid, int* status,
+                           cudaStream_t s);
 cudaError_t launch_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,
-                          float* dst, cudaStream_t s);
+                          float* dst, int32_t* status, cudaStream_t s);
 cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N,
                               const float* a, const float* b, const float* c, const float* d,
-                              float* a_c, float* b_c, float* c_c, float* d_c, cudaStream_t s);
+                              float* a_c, float* b_c, float* c_c, float* d_c, int* status,
+                              cudaStream_t s);
 // Sum of the dHidden K-split partials of one chunk, rows scattered to
 // dhidden[idx] as bf16; does nothing when the contraction was not split.
 cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
                              int chunk_rows, int H, int tile_m, int workers, int num_kb,
                              int max_split, int fill_pct, const int32_t* idx,
-                             const uint8_t* lvalid, __nv_bfloat16* dhidden, cudaStream_t s);
+                             const uint8_t* lvalid, __nv_bfloat16* dhidden, int64_t N,
+                             int* status, cudaStream_t s);
 cudaError_t launch_zero_skipped_rows(const uint8_t* keep, int64_t N, int H,
                                      __nv_bfloat16* dhidden, cudaStream_t s);
 

@@ -378,6 +378,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.chunk_rows = static_cast<int>(L.C);
   p.V = V;
   p.H = H;
+  p.n_rows = N;
   p.group_m = row_block_tiles(H, pair ? 256 : kBM, L.C);
   p.group_n = 16;
   p.status = status;
@@ -394,7 +395,8 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
     if (!blocksparse) {
       Launch l(kKindGatherRows, s);
       LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
-                                static_cast<int>(c), static_cast<int>(L.C), H, hc, s));
+                                static_cast<int>(c), static_cast<int>(L.C), H, hc, N, status,
+                                s));
     }
     p.chunk_index = static_cast<int>(c);
     {
@@ -410,10 +412,11 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   {
     Launch l(kKindExpand, s);
     if (partial != nullptr) {
-      LM_TRY(launch_expand4(keep, idx, d_nk, N, raw_c, partial, s));
+      LM_TRY(launch_expand4(keep, idx, d_nk, N, raw_c, partial, status, s));
     } else {
       LM_TRY(launch_expand3(keep, idx, d_nk, N, lp_c, want_entropy ? ent_c : nullptr, lse_c,
-                            logprob, want_entropy ? entropy : nullptr, lse, lvalid, s));
+                            logprob, want_entropy ? entropy : nullptr, lse, lvalid, status,
+                            s));
     }
   }
   return LMHEAD_OK;
@@ -479,7 +482,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   {
     Launch l(kKindGatherVec, s);
     LM_TRY(launch_gather_vec(idx, d_nk, N, lse, grad_entropy ? entropy : nullptr, grad_logprob,
-                             grad_entropy, lse_c, ent_c, glp_c, gent_c, s));
+                             grad_entropy, lse_c, ent_c, glp_c, gent_c, status, s));
   }
   if (keep != nullptr) {
     Launch l(kKindZeroRows, s);
@@ -506,6 +509,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.chunk_rows = static_cast<int>(L.C);
   p.V = V;
   p.H = H;
+  p.n_rows = N;
   p.status = status;
   p.stall = fault_at("stall") ? 1 : 0;
   p.targets_c = yc;
@@ -531,7 +535,8 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     if (!blocksparse) {
       Launch l(kKindGatherRows, s);
       LM_TRY(launch_gather_rows(static_cast<const __nv_bfloat16*>(hidden), idx, d_nk,
-                                static_cast<int>(c), static_cast<int>(L.C), H, hc, s));
+                                static_cast<int>(c), static_cast<int>(L.C), H, hc, N, status,
+                                s));
     }
     {
       Launch l(kKindGemmDz, s);
@@ -550,7 +555,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       LM_TRY(launch_dh_reduce(p.dh_part, d_nk, static_cast<int>(c), static_cast<int>(L.C), H,
                               pair ? 256 : kBM, dh_workers, static_cast<int>(cdiv(V, kBK)),
                               p.max_split, p.split_fill_pct, idx, lvalid,
-                              static_cast<__nv_bfloat16*>(dhidden), s));
+                              static_cast<__nv_bfloat16*>(dhidden), N, status, s));
     }
     {
       Launch l(kKindGemmDw, s);
@@ -696,15 +701,15 @@ lmhead_status lmhead_bwd_shard(const void* hidden, const void* weight_shard,
 }
 
 lmhead_status lmhead_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,
-                            float* dst, lmhead_stream_t stream) {
+                            float* dst, int32_t* d_status, lmhead_stream_t stream) {
   if (N < 0 || src == nullptr || idx == nullptr || d_nk == nullptr || dst == nullptr)
     return LMHEAD_EINVAL;
   if (N == 0) return LMHEAD_OK;
   if (!device_info().ok) return LMHEAD_EUNSUPPORTED;
-  LM_CHECK_PTRS(src, idx, d_nk, dst);
+  LM_CHECK_PTRS(src, idx, d_nk, dst, d_status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Launch l(kKindExpand, s);
-  return cuda_status(launch_expand(src, idx, d_nk, N, dst, s));
+  return cuda_status(launch_expand(src, idx, d_nk, N, dst, d_status, s));
 }
 
 lmhead_status lmhead_selective_log_softmax_fwd(const void* logits, int logits_dtype, int64_t ld,
@@ -776,6 +781,7 @@ const char* lmhead_strerror(lmhead_status status) {
     case LMHEAD_ECUDA: return "CUDA runtime error";
     case LMHEAD_ETIMEOUT: return "device pipeline wait timed out";
     case LMHEAD_EUNSUPPORTED: return "device is not an sm_103 GPU";
+    case LMHEAD_EBOUNDS: return "an index outside its array was skipped";
   }
   return "unknown status";
 }
@@ -815,6 +821,12 @@ lmhead_status lmhead_profile_read(int64_t* launches, double* total_ms) {
 
 int64_t lmhead_launch_count(void) { return g_launches.load(); }
 
-const char* lmhead_version(void) { return "lmhead-gb300 0.1.0 (sm_103a, tcgen05)"; }
+const char* lmhead_version(void) {
+#ifdef LMHEAD_DEBUG
+  return "lmhead-gb300 0.1.0 (sm_103a, tcgen05, debug index checks)";
+#else
+  return "lmhead-gb300 0.1.0 (sm_103a, tcgen05)";
+#endif
+}
 
 }  // extern "C"

@@ -12,6 +12,7 @@ namespace lmhead {
 
 constexpr int kStatusTimeout = 5;   // == LMHEAD_ETIMEOUT
 constexpr int kStatusTarget = 3;    // == LMHEAD_ETARGET
+constexpr int kStatusBounds = 7;    // == LMHEAD_EBOUNDS
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

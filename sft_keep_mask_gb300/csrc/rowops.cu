@@ -157,7 +157,9 @@ __global__ void tile_rows_kernel(const uint8_t* __restrict__ keep,
   const int64_t l = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (l == 0) *d_nk = na * 256;
   if (l >= static_cast<int64_t>(na) * 256) return;
-  const int64_t r = static_cast<int64_t>(tile_list[l >> 8]) * 256 + (l & 255);
+  const int64_t tile = tile_list[l >> 8];
+  if (!LM_DCHECK(tile >= 0 && tile * 256 < N, status)) return;
+  const int64_t r = tile * 256 + (l & 255);
   const bool kept = r < N && (keep == nullptr || keep[r] != 0);
   int64_t y = 0;
   if (kept) {
@@ -179,7 +181,7 @@ __global__ void tile_rows_kernel(const uint8_t* __restrict__ keep,
 __global__ void gather_rows_kernel(const uint4* __restrict__ hidden,
                                    const int32_t* __restrict__ idx, const int32_t* d_nk,
                                    int chunk_index, int chunk_rows, int vec_per_row,
-                                   uint4* __restrict__ hc) {
+                                   uint4* __restrict__ hc, int64_t N, int* status) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   const int padded = (rows + 255) & ~255;
@@ -188,7 +190,9 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ hidden,
   if (r >= padded || rows == 0) return;
   uint4* dst = hc + static_cast<int64_t>(r) * vec_per_row;
   if (r < rows) {
-    const uint4* src = hidden + static_cast<int64_t>(idx[chunk_start + r]) * vec_per_row;
+    const int32_t row = idx[chunk_start + r];
+    if (!LM_DCHECK(row >= 0 && row < N, status)) return;
+    const uint4* src = hidden + static_cast<int64_t>(row) * vec_per_row;
     for (int v = l; v < vec_per_row; v += 32) dst[v] = src[v];
   } else {
     for (int v = l; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
@@ -197,10 +201,12 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ hidden,
 
 __global__ void gather_vec_kernel(const int32_t* __restrict__ idx, const int32_t* d_nk,
                                   const float* a, const float* b, const float* c, const float* d,
-                                  float* a_c, float* b_c, float* c_c, float* d_c) {
+                                  float* a_c, float* b_c, float* c_c, float* d_c, int64_t N,
+                                  int* status) {
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= *d_nk) return;
   const int r = idx[k];
+  if (!LM_DCHECK(r >= 0 && r < N, status)) return;
   if (a) a_c[k] = a[r];
   if (b) b_c[k] = b[r];
   if (c) c_c[k] = c[r];
@@ -322,11 +328,14 @@ __global__ void merge_shards_kernel(const float4* __restrict__ partials, int num
 // Expand compact float4 rows to all rows; skipped rows get (-inf, 0, 0, -inf).
 __global__ void expand4_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ idx,
                                const int32_t* d_nk, int64_t N, const float4* __restrict__ src,
-                               float4* __restrict__ dst) {
+                               float4* __restrict__ dst, int* status) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= N) return;
   if (keep != nullptr && keep[i] == 0) dst[i] = make_float4(-INFINITY, 0.f, 0.f, -INFINITY);
-  if (i < *d_nk) dst[idx[i]] = src[i];
+  if (i < *d_nk) {
+    const int32_t r = idx[i];
+    if (LM_DCHECK(r >= 0 && r < N, status)) dst[r] = src[i];
+  }
 }
 
 // ------------------------------------------------------------------- expand
@@ -335,7 +344,7 @@ __global__ void expand4_kernel(const uint8_t* __restrict__ keep, const int32_t* 
 __global__ void expand3_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ idx,
                                const int32_t* d_nk, int64_t N, const float* a_c,
                                const float* b_c, const float* c_c, float* a, float* b,
-                               float* c, const uint8_t* __restrict__ lvalid) {
+                               float* c, const uint8_t* __restrict__ lvalid, int* status) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < N && keep != nullptr && keep[i] == 0) {
     if (a) a[i] = 0.f;
@@ -344,23 +353,36 @@ __global__ void expand3_kernel(const uint8_t* __restrict__ keep, const int32_t* 
   }
   if (i < *d_nk && (lvalid == nullptr || lvalid[i] != 0)) {
     const int r = idx[i];
+    if (!LM_DCHECK(r >= 0 && r < N, status)) return;
     if (a) a[r] = a_c[i];
     if (b) b[r] = b_c[i];
     if (c) c[r] = c_c[i];
   }
 }
 
+// The public expansion: idx and Nk come from the caller, so an index outside
+// [0, N) (or Nk > N) is skipped and reported instead of written.
 __global__ void scatter_vals_kernel(const float* __restrict__ src, const int32_t* __restrict__ idx,
-                                    const int32_t* d_nk, float* __restrict__ dst) {
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k < *d_nk) dst[idx[k]] = src[k];
+                                    const int32_t* d_nk, int64_t N, float* __restrict__ dst,
+                                    int* status) {
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nk = *d_nk;
+  if (k == 0 && nk > N && status != nullptr) atomicCAS(status, 0, kStatusBounds);
+  if (k >= nk || k >= N) return;
+  const int32_t r = idx[k];
+  if (r < 0 || r >= N) {
+    if (status != nullptr) atomicCAS(status, 0, kStatusBounds);
+    return;
+  }
+  dst[r] = src[k];
 }
 
 __global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t* d_nk,
                                  int chunk_index, int chunk_rows, int H, int tile_m, int workers,
                                  int num_kb, int max_split, int fill_pct,
                                  const int32_t* __restrict__ idx,
-                                 const uint8_t* __restrict__ lvalid, uint2* __restrict__ dhidden) {
+                                 const uint8_t* __restrict__ lvalid, uint2* __restrict__ dhidden,
+                                 int64_t N, int* status) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   if (rows == 0) return;
@@ -389,6 +411,7 @@ __global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t*
       }
     }
     const int64_t orow = idx[chunk_start + r];
+    if (!LM_DCHECK(orow >= 0 && orow < N, status)) continue;
     dhidden[orow * q + c] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
 }
@@ -446,11 +469,11 @@ cudaError_t launch_tile_scan(const uint8_t* keep, const int64_t* targets, int64_
 
 cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
                                const int32_t* d_nk, int chunk_index, int chunk_rows, int H,
-                               __nv_bfloat16* hc, cudaStream_t s) {
+                               __nv_bfloat16* hc, int64_t N, int* status, cudaStream_t s) {
   const int vec = H / 8;
   gather_rows_kernel<<<blocks_for(chunk_rows, 8), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(hidden), idx, d_nk, chunk_index, chunk_rows, vec,
-      reinterpret_cast<uint4*>(hc));
+      reinterpret_cast<uint4*>(hc), N, status);
   return cudaGetLastError();
 }
 
@@ -473,40 +496,42 @@ cudaError_t launch_merge_shards(const float4* partials, int num_shards, const ui
 }
 
 cudaError_t launch_expand4(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk, int64_t N,
-                           const float4* src, float4* dst, cudaStream_t s) {
-  expand4_kernel<<<blocks_for(N, 256), 256, 0, s>>>(keep, idx, d_nk, N, src, dst);
+                           const float4* src, float4* dst, int* status, cudaStream_t s) {
+  expand4_kernel<<<blocks_for(N, 256), 256, 0, s>>>(keep, idx, d_nk, N, src, dst, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_expand3(const uint8_t* keep, const int32_t* idx, const int32_t* d_nk,
                            int64_t N, const float* a_c, const float* b_c, const float* c_c,
-                           float* a, float* b, float* c, const uint8_t* lvalid, cudaStream_t s) {
+                           float* a, float* b, float* c, const uint8_t* lvalid, int* status,
+                           cudaStream_t s) {
   // compact rows may reach N rounded up to 256 in block-sparse mode
   expand3_kernel<<<blocks_for((N + 255) / 256 * 256, 256), 256, 0, s>>>(
-      keep, idx, d_nk, N, a_c, b_c, c_c, a, b, c, lvalid);
+      keep, idx, d_nk, N, a_c, b_c, c_c, a, b, c, lvalid, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_expand(const float* src, const int32_t* idx, const int32_t* d_nk, int64_t N,
-                          float* dst, cudaStream_t s) {
+                          float* dst, int32_t* status, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(dst, 0, static_cast<size_t>(N) * sizeof(float), s);
   if (e != cudaSuccess) return e;
-  scatter_vals_kernel<<<blocks_for(N, 256), 256, 0, s>>>(src, idx, d_nk, dst);
+  scatter_vals_kernel<<<blocks_for(N, 256), 256, 0, s>>>(src, idx, d_nk, N, dst, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N, const float* a,
                               const float* b, const float* c, const float* d, float* a_c,
-                              float* b_c, float* c_c, float* d_c, cudaStream_t s) {
-  gather_vec_kernel<<<blocks_for((N + 255) / 256 * 256, 256), 256, 0, s>>>(idx, d_nk, a, b, c, d,
-                                                                         a_c, b_c, c_c, d_c);
+                              float* b_c, float* c_c, float* d_c, int* status, cudaStream_t s) {
+  gather_vec_kernel<<<blocks_for((N + 255) / 256 * 256, 256), 256, 0, s>>>(
+      idx, d_nk, a, b, c, d, a_c, b_c, c_c, d_c, N, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
                              int chunk_rows, int H, int tile_m, int workers, int num_kb,
                              int max_split, int fill_pct, const int32_t* idx,
-                             const uint8_t* lvalid, __nv_bfloat16* dhidden, cudaStream_t s) {
+                             const uint8_t* lvalid, __nv_bfloat16* dhidden, int64_t N,
+                             int* status, cudaStream_t s) {
   // a grid-stride loop over a grid of 4 blocks per SM: cheap when the
   // contraction was not split and the kernel returns at once
   const int64_t threads = static_cast<int64_t>(chunk_rows) * (H / 4);
@@ -514,7 +539,7 @@ cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_i
   const unsigned cap = static_cast<unsigned>(4 * (device_sm_count() > 0 ? device_sm_count() : 148));
   dh_reduce_kernel<<<want < cap ? want : cap, 256, 0, s>>>(
       reinterpret_cast<const float4*>(part), d_nk, chunk_index, chunk_rows, H, tile_m, workers,
-      num_kb, max_split, fill_pct, idx, lvalid, reinterpret_cast<uint2*>(dhidden));
+      num_kb, max_split, fill_pct, idx, lvalid, reinterpret_cast<uint2*>(dhidden), N, status);
   return cudaGetLastError();
 }
 

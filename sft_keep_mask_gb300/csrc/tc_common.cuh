@@ -195,7 +195,7 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
         }
       }
     }
-    if (row_ok)
+    if (row_ok && LM_DCHECK(row < p.chunk_rows, p.status))
       p.part[static_cast<int64_t>(nt) * p.chunk_rows + row] =
           make_float4(m2 * kLn2, s, u2 * kLn2, tz);
   } else if (MODE == kDz) {
@@ -260,8 +260,9 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
       if (c & 1) out_issue(os, b, lane, box_col, row0, false);
     }
   } else if (MODE == kDh) {
-    const bool row_ok = row < rows_valid && (p.lvalid == nullptr || p.lvalid[cstart + row] != 0);
-    const int64_t orow = row_ok ? p.idx[cstart + row] : 0;
+    const bool kept = row < rows_valid && (p.lvalid == nullptr || p.lvalid[cstart + row] != 0);
+    const int64_t orow = kept ? p.idx[cstart + row] : 0;
+    const bool row_ok = kept && LM_DCHECK(orow >= 0 && orow < p.n_rows, p.status);
     __nv_bfloat16* hrow = p.dhidden + orow * p.H;
     float* prow = p.dh_part +
                   (static_cast<int64_t>(split_idx) * p.chunk_rows + (row_ok ? row : 0)) * p.H;

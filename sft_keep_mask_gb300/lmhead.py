@@ -14,7 +14,10 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "liblmhead.so")
+# LMHEAD_LIBRARY=debug selects the build with device-side index checks.
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
+                         "liblmhead_debug.so" if os.environ.get("LMHEAD_LIBRARY") == "debug"
+                         else "liblmhead.so")
 _lib = None
 
 LMHEAD_OK = 0
@@ -24,6 +27,7 @@ LMHEAD_ETARGET = 3
 LMHEAD_ECUDA = 4
 LMHEAD_ETIMEOUT = 5
 LMHEAD_EUNSUPPORTED = 6
+LMHEAD_EBOUNDS = 7
 DEFAULT_CHUNK_ROWS = 8192
 
 
@@ -44,7 +48,7 @@ _SIGS = {
                           ctypes.c_size_t, _VP]),
     "lmhead_bwd": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
                           _I32, _I32, _VP, ctypes.c_size_t, _VP]),
-    "lmhead_expand": (_I32, [_VP, _VP, _VP, _I64, _VP, _VP]),
+    "lmhead_expand": (_I32, [_VP, _VP, _VP, _I64, _VP, _VP, _VP]),
     "lmhead_fwd_blocksparse": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _VP, _VP, _VP,
                                       _I32, _VP, ctypes.c_size_t, _VP]),
     "lmhead_bwd_blocksparse": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
@@ -292,13 +296,14 @@ def lmhead_bwd_shard(hidden, weight_shard, v_begin, V_total, targets, keep, lse,
     _check(code, "lmhead_bwd_shard")
 
 
-def lmhead_expand(src, idx, d_nk, N, dst, stream=None):
+def lmhead_expand(src, idx, d_nk, N, dst, d_status=None, stream=None):
     _need(src, torch.float32, "src")
     _need(idx, torch.int32, "idx")
     _need(d_nk, torch.int32, "d_nk", 1)
     _need(dst, torch.float32, "dst", N)
-    code = _call("lmhead_expand", (src, idx, d_nk, dst), _p(src), _p(idx), _p(d_nk), N, _p(dst),
-                 stream=stream)
+    _need(d_status, torch.int32, "d_status", 1)
+    code = _call("lmhead_expand", (src, idx, d_nk, dst, d_status), _p(src), _p(idx), _p(d_nk), N,
+                 _p(dst), _p(d_status), stream=stream)
     _check(code, "lmhead_expand")
 
 

@@ -100,7 +100,7 @@ def test_bad_arguments_return_einval_without_a_device(L):
     assert L.lmhead_bwd(_fake(), _fake(), _fake(), None, N, H, V, _fake(), _fake(), _fake(),
                         _fake(), _fake(), None, 0, 0, ws, big, None) == 1
     # expand / compact / keep mask argument checks
-    assert L.lmhead_expand(None, _fake(), _fake(), N, _fake(), None) == 1
+    assert L.lmhead_expand(None, _fake(), _fake(), N, _fake(), None, None) == 1
     assert L.lmhead_compact(None, None, N, V, _fake(), _fake(), _fake(), ws, big, None) == 1
     assert L.lmhead_build_keep_mask(None, None, None, None, 1, N, _fake(), None) == 1
 

@@ -449,3 +449,37 @@ def test_wide_hidden_and_long_vocabulary(monkeypatch, variant):
     monkeypatch.setenv("LMHEAD_GEMM", variant)
     _run_both(synth.workload("tiny", seed=510, N=520, H=8192, V=3000), chunk_rows=256)
     _run_both(synth.workload("tiny", seed=511, N=96, H=256, V=200000), chunk_rows=256)
+
+
+def test_expand_skips_and_reports_out_of_range_indices():
+    # lmhead_expand takes idx and Nk from the caller: entries outside [0, N)
+    # (and Nk > N) are skipped and reported as LMHEAD_EBOUNDS.  dst sits inside
+    # a larger guarded buffer, so nothing lands outside memory the test owns.
+    n, guard = 100, 64
+    buf = torch.full((n + 2 * guard,), -5.0, device=DEV)
+    dst = buf[guard:guard + n]
+    src = torch.arange(1, 9, dtype=torch.float32, device=DEV)
+    idx = torch.tensor([3, -1, 50, n, 99, n + 5, 0, 7], dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.lmhead_expand(src, idx, torch.tensor([8], dtype=torch.int32, device=DEV), n, dst, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == L.LMHEAD_EBOUNDS
+    want = np.zeros(n, np.float32)
+    for k, r in enumerate(idx.tolist()):
+        if 0 <= r < n:
+            want[r] = k + 1
+    np.testing.assert_array_equal(dst.cpu().numpy(), want)
+    assert (buf[:guard] == -5.0).all() and (buf[guard + n:] == -5.0).all()
+    # Nk larger than N: the first N entries are expanded and the excess reported
+    st.zero_()
+    src2 = torch.arange(1, n + 1, dtype=torch.float32, device=DEV)
+    idx2 = torch.arange(n - 1, -1, -1, dtype=torch.int32, device=DEV)
+    L.lmhead_expand(src2, idx2, torch.tensor([n + 40], dtype=torch.int32, device=DEV), n, dst, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == L.LMHEAD_EBOUNDS
+    np.testing.assert_array_equal(dst.cpu().numpy(), np.arange(n, 0, -1, dtype=np.float32))
+    # valid input leaves the status word alone
+    st.zero_()
+    L.lmhead_expand(src2, idx2, torch.tensor([n], dtype=torch.int32, device=DEV), n, dst, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0

@@ -26,8 +26,10 @@ def test_shards_merge_to_the_whole_vocabulary(bounds):
     N, H, V = w.N, w.H, w.V
     shards = list(zip(bounds[:-1], bounds[1:]))
     parts = torch.empty(len(shards), N, 4, device=DEV)
+    scorers = []
     for r, (a, b) in enumerate(shards):
         sc = LMHeadScorer(N, H, b - a, chunk_rows=256)
+        scorers.append(sc)
         Wr = inp["weight"][a:b].contiguous()
         L.lmhead_fwd_shard(inp["hidden"], Wr, a, V, inp["targets"], keep, True, parts[r],
                            sc.workspace, 256)
@@ -39,6 +41,7 @@ def test_shards_merge_to_the_whole_vocabulary(bounds):
     dW = torch.empty(V, H, device=DEV)
     for r, (a, b) in enumerate(shards):
         sc = LMHeadScorer(N, H, b - a, chunk_rows=256)
+        scorers.append(sc)
         Wr = inp["weight"][a:b].contiguous()
         dh_r = torch.empty(N, H, dtype=torch.bfloat16, device=DEV)
         L.lmhead_bwd_shard(inp["hidden"], Wr, a, V, inp["targets"], keep, lse, ent,
@@ -46,6 +49,7 @@ def test_shards_merge_to_the_whole_vocabulary(bounds):
                            sc.workspace, 256)
         dh += dh_r.float()  # the caller's reduction over shards
     torch.cuda.synchronize()
+    assert all(sc.status() == 0 for sc in scorers)
     h, W = to64(inp["hidden"]), to64(inp["weight"])
     y = inp["targets"].cpu().numpy()
     k = keep.cpu().numpy()
