@@ -170,3 +170,41 @@ def test_one_scorer_serves_smaller_batches():
     inp = synth.make_inputs(w, device=DEV)
     with pytest.raises(ValueError, match="capacity"):
         big.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
+
+
+_ALLOC_SCRIPT = """
+import torch
+from sft_keep_mask_gb300 import synth
+from sft_keep_mask_gb300.api import LMHeadScorer
+w = synth.workload("tiny", seed=5, N=600, H=128, V=2000)
+inp = synth.make_inputs(w, device="cuda")
+sc = LMHeadScorer(w.N, w.H, w.V)
+lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
+dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"], lse, ent,
+                     inp["grad_logprob"], inp["grad_entropy"])
+torch.cuda.synchronize()
+assert sc.status() == 0
+print(repr(float(lp.double().sum())), repr(float(dW.double().abs().sum())))
+"""
+
+
+def test_memory_from_every_torch_allocator_mode_is_accepted():
+    # the entry points refuse pointers that are not device memory of the
+    # current device; tensors from the expandable-segment (virtual memory)
+    # and cudaMallocAsync allocators are device memory and must pass, with
+    # the same results as the default allocator
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for conf in (None, "expandable_segments:True", "backend:cudaMallocAsync"):
+        env = dict(os.environ)
+        env.pop("PYTORCH_CUDA_ALLOC_CONF", None)
+        if conf:
+            env["PYTORCH_CUDA_ALLOC_CONF"] = conf
+        r = subprocess.run([sys.executable, "-c", _ALLOC_SCRIPT], env=env, cwd=root,
+                           capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, (conf, r.stderr[-2000:])
+        outs.append(r.stdout.strip().splitlines()[-1])
+    assert len(set(outs)) == 1, outs
