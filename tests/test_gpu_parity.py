@@ -483,3 +483,9 @@ def test_expand_skips_and_reports_out_of_range_indices():
     L.lmhead_expand(src2, idx2, torch.tensor([n], dtype=torch.int32, device=DEV), n, dst, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+
+
+def test_millions_of_rows_and_a_hundred_chunks():
+    # N = 2.1 M rows (513 compaction blocks), about 1.05 M kept rows in 129
+    # chunks of 8192, with a tiny head so the oracle stays cheap
+    _run_both(synth.workload("tiny", seed=520, N=2_100_000, H=8, V=20))
