@@ -489,3 +489,40 @@ def test_millions_of_rows_and_a_hundred_chunks():
     # N = 2.1 M rows (513 compaction blocks), about 1.05 M kept rows in 129
     # chunks of 8192, with a tiny head so the oracle stays cheap
     _run_both(synth.workload("tiny", seed=520, N=2_100_000, H=8, V=20))
+
+
+def test_numerical_extremes():
+    N, H, V = 300, 64, 1000
+    sc = LMHeadScorer(N, H, V, chunk_rows=256)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(530)
+    h = torch.randn(N, H, generator=g, device=DEV).to(torch.bfloat16)
+    y = torch.randint(0, V, (N,), generator=g, device=DEV)
+    y[0], y[1] = 0, V - 1  # the first and last vocabulary ids
+    keep = torch.ones(N, dtype=torch.uint8, device=DEV)
+    # identical W rows: every logit of a row is equal -> uniform distribution
+    Wu = torch.randn(1, H, generator=g, device=DEV).repeat(V, 1).to(torch.bfloat16)
+    lp, ent, lse = sc.forward(h, Wu, y, keep)
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    np.testing.assert_allclose(lp.cpu().numpy(), -np.log(V), atol=1e-4)
+    np.testing.assert_allclose(ent.cpu().numpy(), np.log(V), atol=1e-4)
+    # very peaked rows (W x 100): logits of order 100, no overflow, lp <= 0,
+    # entropy >= 0, and the oracle's values
+    Wp = (torch.randn(V, H, generator=g, device=DEV) * (100.0 / np.sqrt(H))).to(torch.bfloat16)
+    lp, ent, lse = sc.forward(h, Wp, y, keep)
+    g_lp = torch.randn(N, generator=g, device=DEV)
+    g_ent = 0.1 * torch.randn(N, generator=g, device=DEV)
+    dh, dW = sc.backward(h, Wp, y, keep, lse, ent, g_lp, g_ent)
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    for t in (lp, ent, lse, dh.float(), dW):
+        assert torch.isfinite(t).all()
+    assert (lp <= 1e-5).all() and (ent >= -1e-5).all()
+    olp, oent, olse = O.forward(to64(h), to64(Wp), y.cpu().numpy(), None)
+    assert_rows_close(lp.cpu().double().numpy(), olp, "logprob")
+    assert_rows_close(ent.cpu().double().numpy(), oent, "entropy")
+    assert_rows_close(lse.cpu().double().numpy(), olse, "lse")
+    odh, odW = O.backward(to64(h), to64(Wp), y.cpu().numpy(), None, to64(g_lp), to64(g_ent))
+    assert_frob_close(to64(dh), odh, "dhidden")
+    assert_frob_close(dW.cpu().double().numpy(), odW, "dW")
