@@ -90,6 +90,11 @@ typedef void* lmhead_stream_t;
  * O(N + C*(H + V)) with C = chunk_rows: it never holds [N, V] logits
  * ([P3] section 1: memory scales with chunks, not with rows).
  * Returns 0 for invalid sizes (N < 0, H or V < 1).
+ * The figure never decreases with N, so a workspace sized for N_max serves
+ * every call with N <= N_max (same H, V, chunk_rows): each call lays the
+ * workspace out from its own N.  Calls that share a workspace must not
+ * overlap on the GPU (order them on one stream): it holds their intermediate
+ * buffers and their status word.
  */
 size_t lmhead_workspace_size(int64_t N, int H, int V, int want_entropy, int chunk_rows);
 
