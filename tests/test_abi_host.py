@@ -142,3 +142,16 @@ def test_binding_runs_each_call_on_its_tensors_device():
     assert lmhead._device_of(None, None) is None
     with pytest.raises(TypeError, match="CUDA"):
         lmhead._device_of(torch.zeros(2))  # host tensors never reach the library
+
+
+def test_workspace_size_never_decreases_with_n(L):
+    # a workspace sized for N_max serves every smaller batch (the header's
+    # promise, which LMHeadScorer and the autograd op rely on)
+    from sft_keep_mask_gb300 import lmhead
+    f = lmhead.lmhead_workspace_size
+    for H, V, C in ((8, 20, 256), (4096, 151936, 0), (192, 3000, 768)):
+        prev = 0
+        for N in list(range(0, 3000, 7)) + [8191, 8192, 8193, 65536, 262144]:
+            cur = f(N, H, V, True, C)
+            assert cur >= prev, (H, V, C, N)
+            prev = cur
