@@ -359,13 +359,18 @@ def run_ours(args):
     launches0 = L.lmhead_launch_count()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    # one event per step boundary as well, for the spread of the step times
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(local) as clk:
         barrier()
         ev0.record(stream)
-        for _ in range(args.steps):
+        marks[0].record(stream)
+        for i in range(args.steps):
             step(*dev_args)
+            marks[i + 1].record(stream)
         ev1.record(stream)
         barrier()
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     L.lmhead_profile_enable(False)
     launches = L.lmhead_launch_count() - launches0
     status_timed = L.lmhead_get_status(ws)
@@ -450,6 +455,8 @@ def run_ours(args):
             "config": run_config(args, N, H, V, nk, world, g_ent is not None),
             "peak_device_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
             "logits_bf16_gb_avoided": N * V * 2 / 1e9,
+            "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms),
+                        "max": max(step_ms)},
             "tflops": tflops, "frac_of_peak": tflops / burst,
             "frac_of_sustained_peak": tflops / sustained,
             "gemm_tflops": gemm_tflops,
