@@ -21,6 +21,13 @@ SUITE = ["tests/test_gpu_parity.py", "tests/test_gpu_shards.py", "tests/test_gpu
          "tests/test_gpu_autograd.py", "tests/test_gpu_runtime.py"]
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _debug_library():
+    # build() makes it; build it here too if it is missing or stale
+    from sft_keep_mask_gb300 import build as b
+    b.build(debug=True)
+
+
 def _env():
     return dict(os.environ, LMHEAD_LIBRARY="debug")
 
