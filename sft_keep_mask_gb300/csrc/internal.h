@@ -31,9 +31,9 @@ inline bool device_ptrs_ok(std::initializer_list<const void*> ptrs) {
 
 // Debug builds (-DLMHEAD_DEBUG): every index the kernels derive from data is
 // checked before the access it guards; a failed check records LMHEAD_EBOUNDS
-// (7) in the status word and the access is skipped.  This stands in for a
-// memory checker that cannot run here.  Release builds compile the checks
-// out (LM_DCHECK is then the constant true).
+// (7) in the status word and the access is skipped, so a wrong index shows up
+// as a status instead of as a stray memory access.  Release builds compile the
+// checks out (LM_DCHECK is then the constant true).
 #ifdef LMHEAD_DEBUG
 __device__ __forceinline__ bool lm_index_ok(bool ok, int* status) {
   if (!ok && status != nullptr) atomicCAS(status, 0, 7);

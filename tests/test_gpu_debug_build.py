@@ -3,7 +3,8 @@
 That build (liblmhead_debug.so, made by build()) checks every index its
 kernels derive from data before the access it guards, and records
 LMHEAD_EBOUNDS in the device status word instead of touching memory outside an
-array: it stands in for a memory checker, which does not run on these GPUs.
+array, so a wrong index becomes a failed status check rather than a stray
+access.
 The suite runs in a child process with LMHEAD_LIBRARY=debug; its tests assert a
 clean device status after their calls and compare with the oracle, so a
 failed index check fails them.
