@@ -208,3 +208,47 @@ def test_memory_from_every_torch_allocator_mode_is_accepted():
         assert r.returncode == 0, (conf, r.stderr[-2000:])
         outs.append(r.stdout.strip().splitlines()[-1])
     assert len(set(outs)) == 1, outs
+
+
+def test_two_host_threads_with_their_own_streams_and_scorers():
+    # ctypes releases the GIL during library calls, so two host threads drive
+    # the library at the same time (the launch counter, profiling records and
+    # the per-device set-up are shared host state); each thread repeats its
+    # own problem on its own stream, and every result must equal a
+    # single-threaded run bit for bit
+    import threading
+    problems = []
+    for seed, (N, H, V) in ((160, (1200, 256, 4000)), (161, (900, 192, 3100))):
+        w = synth.workload("tiny", seed=seed, N=N, H=H, V=V)
+        inp = synth.make_inputs(w, device=DEV)
+        sc = LMHeadScorer(N, H, V, chunk_rows=256)
+        ref = [t.clone() for t in _step_outputs(sc, inp)]
+        problems.append((sc, inp, ref))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(sc, inp, ref):
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.default_stream())
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    got = _step_outputs(sc, inp)
+                    s.synchronize()
+                    if sc.status() != 0 or not all(torch.equal(a, b) for a, b in zip(got, ref)):
+                        errors.append("mismatch")
+                        return
+        except Exception as e:  # surfaced by the assertion below
+            errors.append(repr(e))
+
+    L.lmhead_profile_enable(True)
+    try:
+        threads = [threading.Thread(target=worker, args=p) for p in problems]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+    finally:
+        L.lmhead_profile_enable(False)
+        L.lmhead_profile_read()
+    assert not errors, errors
