@@ -287,24 +287,20 @@ def test_single_cta_variant_empty_and_single_row(single_cta):
     _run_both(w, keep_override=np.zeros(64, np.uint8))
 
 
-def test_variants_agree_bitwise():
+def test_variants_agree_bitwise(monkeypatch):
     # the pair and one-CTA kernels accumulate every logit over K in the same
     # order, so their outputs agree bit for bit
-    import os
     w = synth.workload("tiny", seed=21, N=900, H=320, V=3000)
     inp = synth.make_inputs(w, device=DEV)
     res = []
     for variant in ("pair", "single"):
-        os.environ["LMHEAD_GEMM"] = variant
-        try:
-            sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
-            lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
-            dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"], lse,
-                                 ent, inp["grad_logprob"], inp["grad_entropy"])
-            torch.cuda.synchronize()
-            res.append((lp, ent, lse, dh, dW))
-        finally:
-            del os.environ["LMHEAD_GEMM"]
+        monkeypatch.setenv("LMHEAD_GEMM", variant)  # the previous value comes back after the test
+        sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
+        lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
+        dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"], lse,
+                             ent, inp["grad_logprob"], inp["grad_entropy"])
+        torch.cuda.synchronize()
+        res.append((lp, ent, lse, dh, dW))
     for a, b in zip(*res):
         assert torch.equal(a, b)
 
@@ -416,11 +412,10 @@ def test_full_size_long_context_sampled():
     assert added < 0.1 * w.N * w.V * 2
 
 
-def test_random_shape_sweep():
+def test_random_shape_sweep(monkeypatch):
     # seeded random problems: shapes, keep densities, chunk sizes, GEMM
     # variant and strategy all vary; every one must match the oracle
     rng = np.random.default_rng(2026)
-    import os
     for case in range(12):
         N = int(rng.integers(1, 1500))
         H = int(rng.choice([8, 16, 64, 136, 256, 520]))
@@ -431,13 +426,9 @@ def test_random_shape_sweep():
         variant = str(rng.choice(["pair", "single"]))
         bs = bool(rng.integers(0, 2))
         ent = bool(rng.integers(0, 2))
-        os.environ["LMHEAD_GEMM"] = variant
-        try:
-            w = synth.workload("tiny", seed=300 + case, N=N, H=H, V=V)
-            _run_both(w, chunk_rows=chunk, keep_override=keep, blocksparse=bs,
-                      grad_entropy=ent)
-        finally:
-            del os.environ["LMHEAD_GEMM"]
+        monkeypatch.setenv("LMHEAD_GEMM", variant)  # restored after the test
+        w = synth.workload("tiny", seed=300 + case, N=N, H=H, V=V)
+        _run_both(w, chunk_rows=chunk, keep_override=keep, blocksparse=bs, grad_entropy=ent)
 
 
 @pytest.mark.parametrize("variant", ["pair", "single"])
