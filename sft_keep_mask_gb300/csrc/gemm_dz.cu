@@ -3,10 +3,13 @@
 // parallel.
 #include "tc_gemm.cuh"
 #include "tc_gemm2.cuh"
+#include "tc_gemm4.cuh"
 
 namespace lmhead {
 template cudaError_t launch_tc_gemm<kDz>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                            const TcGemmParams&, int, cudaStream_t);
 template cudaError_t launch_tc_gemm_pair<kDz>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                 const TcGemmParams&, int, cudaStream_t);
+template cudaError_t launch_tc_gemm_quad<kDz>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                const TcGemmParams&, int64_t, cudaStream_t, int*);
 }  // namespace lmhead

@@ -120,6 +120,15 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma
                                 const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
                                 cudaStream_t stream);
 
+// The same contractions on clusters of two CTA pairs that share A by TMA
+// multicast (tc_gemm4.cuh): `units` = row tiles x column-tile pairs (x the
+// largest dHidden K split); A maps use 64-row boxes (K-major A).  The
+// clusters launched go to *clusters_out (the workers of the split rule).
+template <int MODE>
+cudaError_t launch_tc_gemm_quad(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
+                                const CUtensorMap& tma_c, const TcGemmParams& p, int64_t units,
+                                cudaStream_t stream, int* clusters_out);
+
 // The Nk kept rows are cut into ceil(Nk / C) chunks of equal size rounded up
 // to 256 rows (so no chunk is much shorter than the others and the per-chunk
 // cost of the weight-gradient update stays hidden behind its MMAs).  Chunk c
@@ -222,7 +231,7 @@ cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N
 // Sum of the dHidden K-split partials of one chunk, rows scattered to
 // dhidden[idx] as bf16; does nothing when the contraction was not split.
 cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
-                             int chunk_rows, int H, int tile_m, int workers, int num_kb,
+                             int chunk_rows, int H, int tile_m, int tile_n, int workers, int num_kb,
                              int max_split, int fill_pct, const int32_t* idx,
                              const uint8_t* lvalid, __nv_bfloat16* dhidden, int64_t N,
                              int* status, cudaStream_t s);

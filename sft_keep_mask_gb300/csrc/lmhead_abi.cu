@@ -19,10 +19,12 @@
 namespace lmhead {
 namespace {
 
-constexpr bool kDefaultPair = true;
 constexpr int kDhMaxSplit = 4;  // largest K split of the dHidden contraction
 static_assert(kDhMaxSplit <= 4, "the dHidden reduction sums at most four partials");
 constexpr int kDhSplitFillPct = 85;  // split only when fewer worker slots than this are busy
+// The same threshold for the four-CTA variant, whose 36 workers leave a
+// larger last-wave gap (7.1 waves of 256 units run as 8).
+constexpr int kDhSplitFillPctQuad = 92;
 // Raster blocks of the vocabulary projections (kFwd, kDz): 32 MB of bf16 Hc
 // rows, but never fewer than 4096 rows.  The block stays in L2 (together with
 // the vocabulary tiles in flight) while W streams past once per block; measured
@@ -281,27 +283,48 @@ int gemm_grid(int64_t tiles) {
   return static_cast<int>(tiles < sms ? (tiles < 1 ? 1 : tiles) : sms);
 }
 
-// GEMM variant: CTA pairs (256 x 256 tiles) unless LMHEAD_GEMM=single asks
-// for the one-CTA kernel (128 x 256 tiles).
-bool use_pair() {
+// GEMM variant of one contraction.  By default dHidden runs on clusters of
+// two CTA pairs that share its A operand (the dZ rows) by TMA multicast and
+// the other three on CTA pairs (256 x 256 tiles): on the fwd + bwd step at
+// H = 4096 and 5120 the shared dZ stream saves 1.3%, while sharing the A
+// operand of the projections or of dW saved nothing.  LMHEAD_GEMM = "single"
+// (one-CTA kernel, 128 x 256 tiles), "pair" or "quad" puts every contraction
+// on one variant.  Block-sparse calls never use the four-CTA variant.
+enum class GemmVariant { kSingle, kPair, kQuad };
+
+GemmVariant gemm_variant(bool blocksparse, int mode) {
   const char* e = std::getenv("LMHEAD_GEMM");
-  if (e == nullptr) return kDefaultPair;
-  return std::strcmp(e, "single") != 0;
+  if (e != nullptr && std::strcmp(e, "single") == 0) return GemmVariant::kSingle;
+  if (e != nullptr && std::strcmp(e, "pair") == 0) return GemmVariant::kPair;
+  const bool quad = e != nullptr && std::strcmp(e, "quad") == 0 ? true : mode == kDh;
+  return quad && !blocksparse ? GemmVariant::kQuad : GemmVariant::kPair;
 }
+
+// Rows of one tile of the selected variant.
+inline int tile_rows(GemmVariant v) { return v == GemmVariant::kSingle ? kBM : 256; }
 
 // Launches one contraction on the selected variant.  m_upper bounds the rows
 // of D (the chunk for kFwd/kDz/kDh, V for kDw); b_single / b_pair are the B
-// maps for the two variants (they differ only for K-major B); c is the output
-// map of kDz / kDw (the other contractions do not read it).
+// maps for the two variants (they differ only for K-major B); a_quad is the A
+// map of the quad variant (64-row boxes for K-major A); c is the output map of
+// kDz / kDw (the other contractions do not read it).
 // *workers receives the number of persistent workers launched (CTA pairs or
 // CTAs), which the dHidden split rule depends on.
 template <int MODE>
-cudaError_t run_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b_single,
-                     const CUtensorMap& b_pair, const CUtensorMap& c, const TcGemmParams& p,
-                     int64_t m_upper, int64_t n, cudaStream_t s, int* workers = nullptr) {
+cudaError_t run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& a_quad,
+                     const CUtensorMap& b_single, const CUtensorMap& b_pair,
+                     const CUtensorMap& c, const TcGemmParams& p, int64_t m_upper, int64_t n,
+                     cudaStream_t s, int* workers = nullptr) {
   if (fault_at("launch")) return cudaErrorLaunchFailure;
   const int split = MODE == kDh ? p.max_split : 1;
-  if (pair) {
+  if (v == GemmVariant::kQuad) {
+    const int64_t units = cdiv(m_upper, 256) * cdiv(cdiv(n, kBN), 2) * split;
+    int clusters = 0;
+    const cudaError_t e = launch_tc_gemm_quad<MODE>(a_quad, b_pair, c, p, units, s, &clusters);
+    if (workers != nullptr) *workers = clusters;
+    return e;
+  }
+  if (v == GemmVariant::kPair) {
     const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, kBN) * split;
     const int64_t pairs = device_info().sms / 2;
     const int64_t w = tiles < pairs ? (tiles < 1 ? 1 : tiles) : pairs;
@@ -365,10 +388,11 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   }
   if (st != LMHEAD_OK) return st;
 
-  const bool pair = use_pair();
-  CUtensorMap ma, mb, mb2;
+  const GemmVariant gv = gemm_variant(blocksparse, kFwd);
+  CUtensorMap ma, ma64, mb, mb2;
   if (!(blocksparse ? make_map(&ma, hidden, N, H, H, kBM, 64)
                     : make_map(&ma, hc, L.C, H, H, kBM, 64)) ||
+      !make_map(&ma64, hc, L.C, H, H, 64, 64) ||
       !make_map(&mb, weight, V, H, H, kBN, 64) ||
       !make_map(&mb2, weight, V, H, H, 128, 64))
     return LMHEAD_ECUDA;
@@ -379,7 +403,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.V = V;
   p.H = H;
   p.n_rows = N;
-  p.group_m = row_block_tiles(H, pair ? 256 : kBM, L.C);
+  p.group_m = row_block_tiles(H, tile_rows(gv), L.C);
   p.group_n = 16;
   p.status = status;
   p.stall = fault_at("stall") ? 1 : 0;
@@ -401,7 +425,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
     p.chunk_index = static_cast<int>(c);
     {
       Launch l(kKindGemmFwd, s);
-      LM_TRY(run_gemm<kFwd>(pair, ma, mb, mb2, ma, p, L.C, V, s));
+      LM_TRY(run_gemm<kFwd>(gv, ma, ma64, mb, mb2, ma, p, L.C, V, s));
     }
     {
       Launch l(kKindMerge, s);
@@ -489,8 +513,11 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     LM_TRY(launch_zero_skipped_rows(keep, N, H, static_cast<__nv_bfloat16*>(dhidden), s));
   }
 
-  const bool pair = use_pair();
-  CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn, m_dz_out, m_dw_out;
+  const GemmVariant gv_dz = gemm_variant(blocksparse, kDz);
+  const GemmVariant gv_dh = gemm_variant(blocksparse, kDh);
+  const GemmVariant gv_dw = gemm_variant(blocksparse, kDw);
+  CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn, m_dz_out, m_dw_out,
+      m_hc_k64, m_dz_k64;
   const void* rows_src = blocksparse ? hidden : static_cast<const void*>(hc);
   const int64_t rows_n = blocksparse ? N : L.C;
   if (!make_map(&m_hc_k, rows_src, rows_n, H, H, kBM, 64) ||  // A of kDz (K-major)
@@ -500,6 +527,8 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       !make_map(&m_w_mn, weight, V, H, H, 64, 64) ||       // B of kDh (MN-major boxes)
       !make_map(&m_dz_mn, dz, L.C, V, L.dz_ld, 64, 64) ||  // A of kDw (MN-major boxes)
       !make_map(&m_hc_mn, rows_src, rows_n, H, H, 64, 64) ||  // B of kDw (MN-major boxes)
+      !make_map(&m_hc_k64, hc, L.C, H, H, 64, 64) ||          // A of kDz, quad variant
+      !make_map(&m_dz_k64, dz, L.C, V, L.dz_ld, 64, 64) ||     // A of kDh, quad variant
       !make_map(&m_dz_out, dz, L.C, V, L.dz_ld, 32, 64) ||   // output of kDz
       !make_map(&m_dw_out, dweight, V, H, H, 32, 32, true))   // output of kDw (fp32)
     return LMHEAD_ECUDA;
@@ -524,7 +553,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.dhidden = static_cast<__nv_bfloat16*>(dhidden);
   p.dh_part = at<float>(workspace, L.dhp);
   p.max_split = kDhMaxSplit;
-  p.split_fill_pct = kDhSplitFillPct;
+  p.split_fill_pct = gv_dh == GemmVariant::kQuad ? kDhSplitFillPctQuad : kDhSplitFillPct;
   int dh_workers = 0;
   const int64_t n_h_tiles = cdiv(H, kBN);
 
@@ -540,20 +569,22 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     }
     {
       Launch l(kKindGemmDz, s);
-      p.group_m = row_block_tiles(H, pair ? 256 : kBM, L.C);
+      p.group_m = row_block_tiles(H, tile_rows(gv_dz), L.C);
       p.group_n = 16;
-      LM_TRY(run_gemm<kDz>(pair, m_hc_k, m_w_k, m_w_k2, m_dz_out, p, L.C, V, s));
+      LM_TRY(run_gemm<kDz>(gv_dz, m_hc_k, m_hc_k64, m_w_k, m_w_k2, m_dz_out, p, L.C, V, s));
     }
     {
       Launch l(kKindGemmDh, s);
       p.group_m = 0;
       p.group_n = static_cast<int>(n_h_tiles);
-      LM_TRY(run_gemm<kDh>(pair, m_dz_k, m_w_mn, m_w_mn, m_dz_k, p, L.C, H, s, &dh_workers));
+      LM_TRY(run_gemm<kDh>(gv_dh, m_dz_k, m_dz_k64, m_w_mn, m_w_mn, m_dz_k, p, L.C, H, s,
+                           &dh_workers));
     }
     {
       Launch l(kKindDhReduce, s);
       LM_TRY(launch_dh_reduce(p.dh_part, d_nk, static_cast<int>(c), static_cast<int>(L.C), H,
-                              pair ? 256 : kBM, dh_workers, static_cast<int>(cdiv(V, kBK)),
+                              tile_rows(gv_dh), gv_dh == GemmVariant::kQuad ? 2 * kBN : kBN,
+                              dh_workers, static_cast<int>(cdiv(V, kBK)),
                               p.max_split, p.split_fill_pct, idx, lvalid,
                               static_cast<__nv_bfloat16*>(dhidden), N, status, s));
     }
@@ -562,7 +593,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       p.group_m = 0;
       p.group_n = static_cast<int>(n_h_tiles);
       p.beta = (c > 0 || dw_accumulate) ? 1 : 0;
-      LM_TRY(run_gemm<kDw>(pair, m_dz_mn, m_hc_mn, m_hc_mn, m_dw_out, p, V, H, s));
+      LM_TRY(run_gemm<kDw>(gv_dw, m_dz_mn, m_dz_mn, m_hc_mn, m_hc_mn, m_dw_out, p, V, H, s));
     }
   }
   return LMHEAD_OK;

@@ -283,6 +283,19 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// The same load multicast to the CTAs of `cta_mask` (same shared-memory
+// offset in each); the completion of the bytes landing in a CTA is counted on
+// the barrier at bar_cluster_addr's offset in the even CTA of that CTA's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map,
+                                                    uint32_t bar_cluster_addr, int x, int y,
+                                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_addr(slot)),

@@ -378,7 +378,8 @@ __global__ void scatter_vals_kernel(const float* __restrict__ src, const int32_t
 }
 
 __global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t* d_nk,
-                                 int chunk_index, int chunk_rows, int H, int tile_m, int workers,
+                                 int chunk_index, int chunk_rows, int H, int tile_m, int tile_n,
+                                 int workers,
                                  int num_kb, int max_split, int fill_pct,
                                  const int32_t* __restrict__ idx,
                                  const uint8_t* __restrict__ lvalid, uint2* __restrict__ dhidden,
@@ -386,7 +387,7 @@ __global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t*
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   if (rows == 0) return;
-  const int tiles = ((rows + tile_m - 1) / tile_m) * ((H + 255) / 256);
+  const int tiles = ((rows + tile_m - 1) / tile_m) * ((H + tile_n - 1) / tile_n);
   const int splits = dh_split_count(tiles, workers, num_kb, max_split, fill_pct);
   if (splits == 1) return;
   const int q = H / 4;  // float4 columns per row
@@ -528,7 +529,7 @@ cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N
 }
 
 cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
-                             int chunk_rows, int H, int tile_m, int workers, int num_kb,
+                             int chunk_rows, int H, int tile_m, int tile_n, int workers, int num_kb,
                              int max_split, int fill_pct, const int32_t* idx,
                              const uint8_t* lvalid, __nv_bfloat16* dhidden, int64_t N,
                              int* status, cudaStream_t s) {
@@ -538,7 +539,7 @@ cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_i
   const unsigned want = blocks_for(threads, 256);
   const unsigned cap = static_cast<unsigned>(4 * (device_sm_count() > 0 ? device_sm_count() : 148));
   dh_reduce_kernel<<<want < cap ? want : cap, 256, 0, s>>>(
-      reinterpret_cast<const float4*>(part), d_nk, chunk_index, chunk_rows, H, tile_m, workers,
+      reinterpret_cast<const float4*>(part), d_nk, chunk_index, chunk_rows, H, tile_m, tile_n, workers,
       num_kb, max_split, fill_pct, idx, lvalid, reinterpret_cast<uint2*>(dhidden), N, status);
   return cudaGetLastError();
 }

@@ -195,7 +195,9 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
         }
       }
     }
-    if (row_ok && LM_DCHECK(row < p.chunk_rows, p.status))
+    // (a column tile past V -- the second pair's tile of a cluster when the
+    // number of vocabulary tiles is odd -- has no partials to write)
+    if (row_ok && col_tile < p.V && LM_DCHECK(row < p.chunk_rows, p.status))
       p.part[static_cast<int64_t>(nt) * p.chunk_rows + row] =
           make_float4(m2 * kLn2, s, u2 * kLn2, tz);
   } else if (MODE == kDz) {

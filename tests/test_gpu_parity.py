@@ -288,12 +288,12 @@ def test_single_cta_variant_empty_and_single_row(single_cta):
 
 
 def test_variants_agree_bitwise(monkeypatch):
-    # the pair and one-CTA kernels accumulate every logit over K in the same
-    # order, so their outputs agree bit for bit
+    # the three kernels accumulate every logit over K in the same order (and
+    # here split dHidden the same way), so their outputs agree bit for bit
     w = synth.workload("tiny", seed=21, N=900, H=320, V=3000)
     inp = synth.make_inputs(w, device=DEV)
     res = []
-    for variant in ("pair", "single"):
+    for variant in ("pair", "single", "quad"):
         monkeypatch.setenv("LMHEAD_GEMM", variant)  # the previous value comes back after the test
         sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
         lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
@@ -301,8 +301,9 @@ def test_variants_agree_bitwise(monkeypatch):
                              ent, inp["grad_logprob"], inp["grad_entropy"])
         torch.cuda.synchronize()
         res.append((lp, ent, lse, dh, dW))
-    for a, b in zip(*res):
-        assert torch.equal(a, b)
+    for other in res[1:]:
+        for a, b in zip(res[0], other):
+            assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("nk", [255, 256, 257, 511, 513, 1000])
@@ -315,7 +316,7 @@ def test_chunk_boundaries(nk):
     _run_both(w, keep_override=keep, chunk_rows=256)
 
 
-@pytest.mark.parametrize("variant", ["pair", "single"])
+@pytest.mark.parametrize("variant", ["pair", "single", "quad"])
 @pytest.mark.parametrize("N,H,V", [(1, 8, 1), (5, 16, 2), (33, 64, 7), (300, 8, 300),
                                    (70, 24, 129)])
 def test_tiny_and_degenerate_shapes(monkeypatch, variant, N, H, V):
@@ -423,7 +424,7 @@ def test_random_shape_sweep(monkeypatch):
         chunk = int(rng.choice([0, 256, 512, 768]))
         density = float(rng.choice([0.0, 0.05, 0.5, 1.0]))
         keep = (rng.random(N) < density).astype(np.uint8)
-        variant = str(rng.choice(["pair", "single"]))
+        variant = str(rng.choice(["pair", "single", "quad"]))
         bs = bool(rng.integers(0, 2))
         ent = bool(rng.integers(0, 2))
         monkeypatch.setenv("LMHEAD_GEMM", variant)  # restored after the test
@@ -431,7 +432,7 @@ def test_random_shape_sweep(monkeypatch):
         _run_both(w, chunk_rows=chunk, keep_override=keep, blocksparse=bs, grad_entropy=ent)
 
 
-@pytest.mark.parametrize("variant", ["pair", "single"])
+@pytest.mark.parametrize("variant", ["pair", "single", "quad"])
 def test_wide_hidden_and_long_vocabulary(monkeypatch, variant):
     # H = 8192: 128 K steps in the projections and 32 column tiles in dHidden
     # and dW; V = 200000: 782 vocabulary tiles ending in a 64-wide tail, so

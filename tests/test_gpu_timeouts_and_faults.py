@@ -51,7 +51,7 @@ def test_host_fault_sites_return_an_error_and_recover(monkeypatch, site):
     _check_forward(w, inp, sc)
 
 
-@pytest.mark.parametrize("variant", ["pair", "single"])
+@pytest.mark.parametrize("variant", ["pair", "single", "quad"])
 def test_stalled_pipeline_times_out_and_the_context_survives(monkeypatch, variant):
     w, inp = _small()
     sc = LMHeadScorer(w.N, w.H, w.V)
