@@ -323,7 +323,7 @@ def run_ours(args):
 
     keep_arg = None if args.keep_off else keep  # keep-off arm: every row scored
 
-    def step(hidden, targets, loss_mask, offs, g_lp, g_e):
+    def step(hidden, targets, loss_mask, offs, g_lp, g_e, mid=None):
         if args.keep_off:
             pass
         elif loss_mask is not None:
@@ -334,6 +334,8 @@ def run_ours(args):
         bwd = L.lmhead_bwd_blocksparse if args.blocksparse else L.lmhead_bwd
         fwd(hidden, inp["weight"], targets, keep_arg, True, lp, ent, lse, ws, args.chunk_rows,
             stream)
+        if mid is not None:
+            mid.record(stream)  # end of the forward pass
         if args.mode == "fwdbwd":
             bwd(hidden, inp["weight"], targets, keep_arg, lse, ent, g_lp, g_e, dh, dW, False, ws,
                 args.chunk_rows, stream)
@@ -361,16 +363,20 @@ def run_ours(args):
     ev1 = torch.cuda.Event(enable_timing=True)
     # one event per step boundary as well, for the spread of the step times
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         barrier()
         ev0.record(stream)
         marks[0].record(stream)
         for i in range(args.steps):
-            step(*dev_args)
+            step(*dev_args, mid=mids[i])
             marks[i + 1].record(stream)
         ev1.record(stream)
         barrier()
     step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
+    # forward (keep mask build included) and backward parts of each step
+    fwd_ms = [marks[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    bwd_ms = [mids[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     L.lmhead_profile_enable(False)
     launches = L.lmhead_launch_count() - launches0
     status_timed = L.lmhead_get_status(ws)
@@ -384,6 +390,10 @@ def run_ours(args):
     per_row = 8.0 if args.mode == "fwdbwd" else 2.0
     flops_step = per_row * nk_total * H * V
     tflops = flops_step * args.steps / sec / 1e12
+    # the same work counted without the backward's recompute of the logits
+    # (2 Nk H V forward + 4 Nk H V backward)
+    per_row_rf = 6.0 if args.mode == "fwdbwd" else 2.0
+    tflops_rf = per_row_rf * nk_total * H * V * args.steps / sec / 1e12
     burst, sustained, hbm, peak_src = _peaks()
 
     # dominant kernel of the step (largest summed device time)
@@ -457,8 +467,11 @@ def run_ours(args):
             "logits_bf16_gb_avoided": N * V * 2 / 1e9,
             "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms),
                         "max": max(step_ms)},
+            "pass_ms": {"fwd": statistics.median(fwd_ms),
+                        "bwd": statistics.median(bwd_ms) if args.mode == "fwdbwd" else None},
             "tflops": tflops, "frac_of_peak": tflops / burst,
             "frac_of_sustained_peak": tflops / sustained,
+            "tflops_recompute_free": tflops_rf,
             "gemm_tflops": gemm_tflops,
             "roofline": roof, "kernels": kernels, "gpu_launches": launches,
             "clocks": clk.summary(), "device_status": status_timed, "e2e": e2e,
