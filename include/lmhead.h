@@ -52,6 +52,16 @@
  *     Results are deterministic: each output element is written once per
  *     launch, and dW's accumulation over chunks adds each element once per
  *     chunk (a TMA reduce-add at L2), chunk after chunk in a fixed order.
+ *   - Environment, read on every call: LMHEAD_GEMM = "single", "pair" or
+ *     "quad" runs all four contractions on the one-CTA (128 x 256 tiles),
+ *     CTA-pair (256 x 256) or four-CTA (two CTA pairs sharing their A operand
+ *     by TMA multicast) tcgen05 kernel; unset, dHidden runs on four CTAs and
+ *     the other three on CTA pairs (block-sparse calls never use four).  The
+ *     variants accumulate in the same order and differ at most by the K split
+ *     of dHidden.  LMHEAD_FAULT = "tensor_map", "launch" or "stall" makes the
+ *     next calls fail on purpose for tests: a tensor-map encode or a launch
+ *     reports LMHEAD_ECUDA, or the GEMM producers issue no loads so that the
+ *     bounded pipeline waits run out (LMHEAD_ETIMEOUT).
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H
