@@ -449,7 +449,7 @@ def run_ours(args):
         # the keep-off arm scores every row (its keep buffer is never filled)
         keep_np = np.ones(N, np.uint8) if args.keep_off else keep.cpu().numpy()
         W64 = inp["weight"].float().cpu().double().numpy()
-        rows = min(args.ref_rows, nk)
+        rows = min(args.cpu_rows, nk)
         rate, dt = cpu_oracle_rate(inp, keep_np, W64, rows, args.mode, g_ent is not None)
         what = "forward + dhidden + dW contribution" if args.mode == "fwdbwd" else "forward"
         cpu = {"value": rate, "unit": UNIT, "cores": _cores(), "kind": "oracle",
@@ -573,7 +573,11 @@ def main():
                     help="score the active 256-row tiles in place instead of compacting")
     ap.add_argument("--active-frac", type=float, default=1.0,
                     help="active suffix fraction of the entropy_bonus workload")
-    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--ref-rows", type=int, default=256,
+                    help="kept rows the oracle scores per step of --impl reference")
+    ap.add_argument("--cpu-rows", type=int, default=1024,
+                    help="kept rows of the cpu_baseline sample (about 12 s of oracle work "
+                         "at the default shape)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
