@@ -3,7 +3,11 @@
 //     the (row tile, column tile) grid for every raster setting in use;
 //   * chunk_span splits Nk kept rows into chunks that cover [0, Nk) in order,
 //     each at most chunk_rows long;
-//   * dh_split_count never splits past the K blocks or the partial buffers.
+//   * dh_split_count never splits past the K blocks or the partial buffers;
+//   * the four-CTA kernel's units (a row tile x a pair of column tiles x a K
+//     part) cover every (row tile, column tile, K part) once, the K parts
+//     partition the K blocks, and dh_reduce_kernel, which counts units as
+//     row tiles x ceil(H / 512), sees the same unit count as the kernel.
 // Prints "ok" and exits 0, or names the first failing case and exits 1.
 #include <cstdio>
 #include <vector>
@@ -28,6 +32,55 @@ static int check_raster(int num_m, int num_n, int group_m, int group_n) {
       return 1;
     }
   }
+  return 0;
+}
+
+// Units of the four-CTA kernel, walked as the kernel walks them.
+static int check_quad_units(int num_m, int num_n, int group_m, int group_n, int splits,
+                            int num_kb) {
+  const int num_np = (num_n + 1) / 2;
+  const int num_base = num_m * num_np;
+  std::vector<int> seen(static_cast<size_t>(num_m) * num_n * splits, 0);
+  std::vector<int> kcover(static_cast<size_t>(num_kb), 0);
+  for (int u = 0; u < num_base * splits; ++u) {
+    const int sidx = u / num_base;
+    const int kb0 = static_cast<int>(static_cast<long long>(sidx) * num_kb / splits);
+    const int kb1 = static_cast<int>(static_cast<long long>(sidx + 1) * num_kb / splits);
+    if (kb1 <= kb0) {
+      std::printf("quad: empty K part %d of %d over %d blocks\n", sidx, splits, num_kb);
+      return 1;
+    }
+    int mt = -1, ntp = -1;
+    tile_coords(u % num_base, num_m, num_np, group_m, group_n, mt, ntp);
+    if (u % num_base == 0)
+      for (int kb = kb0; kb < kb1; ++kb) ++kcover[static_cast<size_t>(kb)];
+    for (int pq = 0; pq < 2; ++pq) {
+      const int nt = 2 * ntp + pq;
+      if (nt >= num_n) {
+        if (pq == 0 || nt > num_n) {  // only the odd last column tile may be missing
+          std::printf("quad: unit %d -> column tile %d of %d\n", u, nt, num_n);
+          return 1;
+        }
+        continue;
+      }
+      if (mt < 0 || mt >= num_m || seen[(static_cast<size_t>(sidx) * num_m + mt) * num_n + nt]++) {
+        std::printf("quad: M=%d N=%d gm=%d gn=%d S=%d unit %d repeats or leaves the grid\n",
+                    num_m, num_n, group_m, group_n, splits, u);
+        return 1;
+      }
+    }
+  }
+  for (int v : seen)
+    if (v != 1) {
+      std::printf("quad: M=%d N=%d gm=%d gn=%d S=%d misses a tile\n", num_m, num_n, group_m,
+                  group_n, splits);
+      return 1;
+    }
+  for (int v : kcover)
+    if (v != 1) {
+      std::printf("quad: K parts of %d blocks in %d parts do not partition\n", num_kb, splits);
+      return 1;
+    }
   return 0;
 }
 
@@ -73,6 +126,23 @@ int main() {
           return 1;
         }
       }
+  for (int m : {1, 2, 15, 29, 33})
+    for (int n : {1, 2, 3, 10, 16, 17, 20})
+      for (int gm : {0, 16})
+        for (int gn : {1, 4, 16})
+          for (int s : {1, 2, 3, 4})
+            for (int kb : {4, 7, 2374})
+              if (check_quad_units(m, n, gm, gn, s, kb)) return 1;
+
+  // dh_reduce_kernel's unit count (tile_m = 256, tile_n = 512) equals the
+  // four-CTA kernel's for every H, so both take the same K split
+  for (int H = 8; H <= 16384; H += 8) {
+    const int num_n = (H + kBN - 1) / kBN;
+    if ((num_n + 1) / 2 != (H + 2 * kBN - 1) / (2 * kBN)) {
+      std::printf("quad unit count differs from the reduction's at H=%d\n", H);
+      return 1;
+    }
+  }
   std::printf("ok\n");
   return 0;
 }
