@@ -27,6 +27,7 @@
 // review accumulated online in a numerically safe form.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -233,16 +234,16 @@ cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                            const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
                            cudaStream_t stream) {
   // the shared-memory opt-in is per device: set it once on each device used
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // zero-initialised (static storage)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gemm_smem_bytes<MODE>());
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   tc_gemm_kernel<MODE><<<grid, kGemmThreads, gemm_smem_bytes<MODE>(), stream>>>(tma_a, tma_b, tma_c,
                                                                               p);

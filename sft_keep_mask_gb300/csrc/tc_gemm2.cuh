@@ -17,6 +17,7 @@
 //               kDz / kDw, issues the warp's TMA output writes
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -243,16 +244,16 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma
                                 const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
                                 cudaStream_t stream) {
   // the shared-memory opt-in is per device: set it once on each device used
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // zero-initialised (static storage)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair_smem_bytes<MODE>());
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   tc_gemm_pair_kernel<MODE><<<grid, kGemmThreads, pair_smem_bytes<MODE>(), stream>>>(tma_a, tma_b,
                                                                                    tma_c, p);

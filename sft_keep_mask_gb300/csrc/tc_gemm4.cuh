@@ -20,6 +20,7 @@
 // counting units of two column tiles and clusters as the workers.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -244,38 +245,38 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kGemmThreads, 1)
 // memory (not every GPC holds a multiple of four SMs), cached per device.
 template <int MODE>
 int quad_max_clusters(int dev) {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];  // zero-initialised (static storage)
   if (dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
+  int n = cached[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(4, 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = quad_smem_bytes<MODE>();
-    int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_quad_kernel<MODE>, &cfg) != cudaSuccess ||
         n < 1) {
       cudaGetLastError();
       return 0;
     }
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_release);
   }
-  return cached[dev];
+  return n;
 }
 
 template <int MODE>
 cudaError_t launch_tc_gemm_quad(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                                 const CUtensorMap& tma_c, const TcGemmParams& p,
                                 int64_t units, cudaStream_t stream, int* clusters_out) {
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // zero-initialised (static storage)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(tc_gemm_quad_kernel<MODE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, quad_smem_bytes<MODE>());
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   const int maxc = quad_max_clusters<MODE>(dev);
   if (maxc < 1) return cudaErrorLaunchOutOfResources;
