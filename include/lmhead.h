@@ -55,8 +55,9 @@
  *   - Environment, read on every call: LMHEAD_GEMM = "single", "pair" or
  *     "quad" runs all four contractions on the one-CTA (128 x 256 tiles),
  *     CTA-pair (256 x 256) or four-CTA (two CTA pairs sharing their A operand
- *     by TMA multicast) tcgen05 kernel; unset, dHidden runs on four CTAs and
- *     the other three on CTA pairs (block-sparse calls never use four).  The
+ *     by TMA multicast) tcgen05 kernel; unset, dHidden runs on four CTAs when
+ *     H spans an even number of 256-column tiles, and everything else on CTA
+ *     pairs (block-sparse calls never use four).  The
  *     variants accumulate in the same order and differ at most by the K split
  *     of dHidden.  LMHEAD_FAULT = "tensor_map", "launch" or "stall" makes the
  *     next calls fail on purpose for tests: a tensor-map encode or a launch

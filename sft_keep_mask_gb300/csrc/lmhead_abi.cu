@@ -287,16 +287,21 @@ int gemm_grid(int64_t tiles) {
 // two CTA pairs that share its A operand (the dZ rows) by TMA multicast and
 // the other three on CTA pairs (256 x 256 tiles): on the fwd + bwd step at
 // H = 4096 and 5120 the shared dZ stream saves 1.3%, while sharing the A
-// operand of the projections or of dW saved nothing.  LMHEAD_GEMM = "single"
-// (one-CTA kernel, 128 x 256 tiles), "pair" or "quad" puts every contraction
-// on one variant.  Block-sparse calls never use the four-CTA variant.
+// operand of the projections or of dW saved nothing.  The two pairs of a
+// cluster take neighbouring column tiles, so dHidden stays on CTA pairs when
+// H spans an odd number of 256-column tiles (the last cluster's second pair
+// would have no tile).  LMHEAD_GEMM = "single" (one-CTA kernel, 128 x 256
+// tiles), "pair" or "quad" puts every contraction on one variant.
+// Block-sparse calls never use the four-CTA variant.
 enum class GemmVariant { kSingle, kPair, kQuad };
 
-GemmVariant gemm_variant(bool blocksparse, int mode) {
+GemmVariant gemm_variant(bool blocksparse, int mode, int H) {
   const char* e = std::getenv("LMHEAD_GEMM");
   if (e != nullptr && std::strcmp(e, "single") == 0) return GemmVariant::kSingle;
   if (e != nullptr && std::strcmp(e, "pair") == 0) return GemmVariant::kPair;
-  const bool quad = e != nullptr && std::strcmp(e, "quad") == 0 ? true : mode == kDh;
+  const bool quad = e != nullptr && std::strcmp(e, "quad") == 0
+                        ? true
+                        : mode == kDh && cdiv(H, kBN) % 2 == 0;
   return quad && !blocksparse ? GemmVariant::kQuad : GemmVariant::kPair;
 }
 
@@ -388,7 +393,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   }
   if (st != LMHEAD_OK) return st;
 
-  const GemmVariant gv = gemm_variant(blocksparse, kFwd);
+  const GemmVariant gv = gemm_variant(blocksparse, kFwd, H);
   CUtensorMap ma, ma64, mb, mb2;
   if (!(blocksparse ? make_map(&ma, hidden, N, H, H, kBM, 64)
                     : make_map(&ma, hc, L.C, H, H, kBM, 64)) ||
@@ -513,9 +518,9 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     LM_TRY(launch_zero_skipped_rows(keep, N, H, static_cast<__nv_bfloat16*>(dhidden), s));
   }
 
-  const GemmVariant gv_dz = gemm_variant(blocksparse, kDz);
-  const GemmVariant gv_dh = gemm_variant(blocksparse, kDh);
-  const GemmVariant gv_dw = gemm_variant(blocksparse, kDw);
+  const GemmVariant gv_dz = gemm_variant(blocksparse, kDz, H);
+  const GemmVariant gv_dh = gemm_variant(blocksparse, kDh, H);
+  const GemmVariant gv_dw = gemm_variant(blocksparse, kDw, H);
   CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn, m_dz_out, m_dw_out,
       m_hc_k64, m_dz_k64;
   const void* rows_src = blocksparse ? hidden : static_cast<const void*>(hc);
