@@ -443,6 +443,16 @@ def test_wide_hidden_and_long_vocabulary(monkeypatch, variant):
     _run_both(synth.workload("tiny", seed=511, N=96, H=256, V=200000), chunk_rows=256)
 
 
+@pytest.mark.parametrize("variant", ["pair", "single", "quad"])
+def test_widest_hidden_and_largest_vocabulary(monkeypatch, variant):
+    # H = 16384: 256 K steps in the projections, 64 column tiles in dHidden
+    # and dW; V = 262144 (a 256K vocabulary): 1024 vocabulary tiles and
+    # 4096 K steps in dHidden
+    monkeypatch.setenv("LMHEAD_GEMM", variant)
+    _run_both(synth.workload("tiny", seed=512, N=300, H=16384, V=1500), chunk_rows=256)
+    _run_both(synth.workload("tiny", seed=513, N=80, H=512, V=262144), chunk_rows=256)
+
+
 def test_expand_skips_and_reports_out_of_range_indices():
     # lmhead_expand takes idx and Nk from the caller: entries outside [0, N)
     # (and Nk > N) are skipped and reported as LMHEAD_EBOUNDS.  dst sits inside
