@@ -18,6 +18,7 @@
 // stream without ordering) race on the shared array: order them.
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/lmhead.h"
@@ -36,8 +37,15 @@ static_assert(LMHEAD_NOALLOC_MAX_ROWS % kNoallocRowsPerBlock == 0,
 // Per-block kept-row counts of the compaction scan (the only scratch).
 static __device__ __align__(256) int32_t g_noalloc_counts[kNoallocMaxBlocks];
 
-// Device address of g_noalloc_counts, looked up once per device.
+// Device address of g_noalloc_counts, looked up once per device and CUDA
+// context.  The address belongs to the module loaded in one context: a
+// caller that makes another context current on the device, or a
+// cudaDeviceReset that destroys the primary context and loads the module
+// again, gets a fresh look-up.  Contexts are told apart by their unique id
+// (cuCtxGetId), which is never reused within a process, so a new context
+// never matches a stale entry even if its handle value repeats.
 struct ScratchAddr {
+  unsigned long long ctx_id = 0;
   int32_t* ptr = nullptr;
   bool ready = false;
 };
@@ -45,21 +53,61 @@ constexpr int kMaxDevices = 64;
 ScratchAddr g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the current CUDA context (driver entry points reached through
+// the runtime, so the library needs no libcuda link).
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr)
+    return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 lmhead_status scratch_for_current_device(int32_t** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return LMHEAD_ECUDA;
   std::lock_guard<std::mutex> g(g_scratch_mu);
-  if (!g_scratch[dev].ready) {
-    void* p = nullptr;
-    // In host code g_noalloc_counts names a host-side shadow, not device
-    // memory; the device address must come from the runtime.
-    if (cudaGetSymbolAddress(&p, g_noalloc_counts) != cudaSuccess || p == nullptr)
-      return LMHEAD_ECUDA;
-    g_scratch[dev].ptr = static_cast<int32_t*>(p);
-    g_scratch[dev].ready = true;
+  ScratchAddr& e = g_scratch[dev];
+  unsigned long long ctx = 0;
+  if (e.ready && current_context_id(&ctx) && ctx == e.ctx_id) {
+    *out = e.ptr;
+    return LMHEAD_OK;
   }
-  *out = g_scratch[dev].ptr;
+  // Set-up for this device and context.  In host code g_noalloc_counts names
+  // a host-side shadow, not device memory; the device address must come from
+  // the runtime (which also makes the device's context current if no context
+  // was yet).
+  e.ready = false;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_counts) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();  // leave no error behind for the next runtime call
+    return LMHEAD_ECUDA;
+  }
+  if (!current_context_id(&ctx)) return LMHEAD_ECUDA;
+  e.ptr = static_cast<int32_t*>(p);
+  e.ctx_id = ctx;
+  e.ready = true;
+  *out = e.ptr;
   return LMHEAD_OK;
 }
 

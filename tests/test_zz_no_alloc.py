@@ -41,9 +41,10 @@ def test_noalloc_compaction_matches_workspace_entry_point():
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rng = np.random.default_rng(2024)
     V = 151936
-    # two calls in a row with different sizes and masks: the second reuses the
-    # scratch the first left behind
-    for call, (n, p_keep) in enumerate([(100003, 0.55), (37000, 0.2)]):
+    # calls in a row with different sizes and masks: each reuses the scratch
+    # the one before left behind; 8192 rows fill exactly two scan blocks of
+    # 4096, so the last block is a full one
+    for call, (n, p_keep) in enumerate([(100003, 0.55), (37000, 0.2), (8192, 0.5)]):
         keep = torch.from_numpy((rng.random(n) < p_keep).astype(np.uint8)).to(DEV)
         y = torch.from_numpy(rng.integers(0, V, n)).to(DEV)
         outs = []
@@ -93,3 +94,20 @@ def test_noalloc_rejects_oversize_and_reports_bad_targets():
     assert fn(_p(keep), _p(y), n, 10, _p(idx), _p(yc), _p(nk), _p(d_st), stream) == 0
     torch.cuda.synchronize()
     assert int(d_st.item()) == 0 and int(nk.item()) == n
+
+
+def test_noalloc_empty_batch_writes_zero_kept_rows():
+    # N = 0 launches nothing: Nk is written as 0 and the status cleared
+    from sft_keep_mask_gb300 import lmhead
+
+    L = lmhead.lib()
+    fn = _noalloc(L)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    one = torch.zeros(1, dtype=torch.int64, device=DEV)  # any device buffer; N = 0 reads none
+    idx = torch.empty(1, dtype=torch.int32, device=DEV)
+    yc = torch.empty(1, dtype=torch.int32, device=DEV)
+    nk = torch.full((1,), 77, dtype=torch.int32, device=DEV)
+    d_st = torch.full((1,), -7, dtype=torch.int32, device=DEV)
+    assert fn(None, _p(one), 0, 10, _p(idx), _p(yc), _p(nk), _p(d_st), stream) == 0
+    torch.cuda.synchronize()
+    assert int(nk.item()) == 0 and int(d_st.item()) == 0
