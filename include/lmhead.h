@@ -35,7 +35,9 @@
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers on the current CUDA device,
  *     allocated and owned by the caller.  The library never allocates device
- *     memory (the caller passes a workspace) and keeps no per-call state.
+ *     memory (the caller passes a workspace) and keeps no per-call state,
+ *     except the library-wide scratch array of lmhead_compact_noalloc
+ *     (described there).
  *     A pointer that is neither device memory of the current device nor
  *     managed memory (a host pointer, another GPU's memory) is refused with
  *     LMHEAD_EINVAL before anything is launched.
@@ -53,11 +55,12 @@
  *     launch, and dW's accumulation over chunks adds each element once per
  *     chunk (a TMA reduce-add at L2), chunk after chunk in a fixed order.
  *   - Environment, read on every call: LMHEAD_GEMM = "single", "pair" or
- *     "quad" runs all four contractions on the one-CTA (128 x 256 tiles),
- *     CTA-pair (256 x 256) or four-CTA (two CTA pairs sharing their A operand
- *     by TMA multicast) tcgen05 kernel; unset, dHidden runs on four CTAs when
- *     H spans an even number of 256-column tiles, and everything else on CTA
- *     pairs (block-sparse calls never use four).  The
+ *     "wide" runs all four contractions on the one-CTA (128 x 256 tiles),
+ *     CTA-pair (256 x 256 tiles, two accumulators) or wide CTA-pair (256 x
+ *     512 tiles, one accumulator) tcgen05 kernel; unset, dHidden runs on wide
+ *     tiles and everything else on 256 x 256 tiles, unless LMHEAD_WIDE names
+ *     the contractions on wide tiles ("fwd,dz,dh,dw" or a subset, "none").
+ *     LMHEAD_DH_SPLIT = 1 .. 4 caps the K split of dHidden (default 4).  The
  *     variants accumulate in the same order and differ at most by the K split
  *     of dHidden.  LMHEAD_FAULT = "tensor_map", "launch" or "stall" makes the
  *     next calls fail on purpose for tests: a tensor-map encode or a launch
@@ -205,8 +208,9 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
  *   argument errors of lmhead_compact), LMHEAD_EUNSUPPORTED off sm_103.
  *
  * The first call on a device looks up the array's device address (a one-time
- * set-up per device, done with that device current); make that first call
- * before any stream capture.  Every call on a device shares the one array and
+ * set-up per device and CUDA context, done with that device current; a new
+ * context on the device, e.g. after cudaDeviceReset, gets a fresh look-up);
+ * make that first call before any stream capture.  Every call on a device shares the one array and
  * it keeps the last call's contents: calls whose work overlaps on the GPU
  * (e.g. on two streams at once) race and must be ordered by the caller.
  */
@@ -339,6 +343,22 @@ lmhead_status lmhead_selective_log_softmax_bwd(const void* logits, int logits_dt
  * LMHEAD_ETIMEOUT (or LMHEAD_ECUDA if the stream reports an error).
  */
 lmhead_status lmhead_get_status(const void* workspace, lmhead_stream_t stream);
+
+/*
+ * Where the last call on this workspace ran out of time, if it did (the
+ * LMHEAD_ETIMEOUT of lmhead_get_status): synchronises `stream` and returns
+ * 0 if no pipeline wait gave up, else (site << 24) | cta with cta the index
+ * of the first CTA whose wait gave up and site the wait --
+ *   1 a TMA producer waiting for a free shared-memory stage,
+ *   2 the MMA issuer waiting for the epilogue to release an accumulator,
+ *   3 the MMA issuer waiting for a filled stage,
+ *   4 an epilogue warp waiting for a finished accumulator,
+ *   5 a producer letting its last loads land before the CTA exits,
+ *   6 the MMA issuer letting its last MMAs finish before the CTA exits.
+ * Returns -1 for a NULL workspace or a failed CUDA call.  A diagnostic: it
+ * names the wait that gave up when a run reports LMHEAD_ETIMEOUT.
+ */
+int32_t lmhead_get_timeout_record(const void* workspace, lmhead_stream_t stream);
 
 /*
  * Device address (int32, 1 element) where lmhead_fwd / lmhead_bwd /

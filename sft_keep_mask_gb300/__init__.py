@@ -23,6 +23,7 @@ from .lmhead import (  # noqa: F401
     lmhead_fwd_blocksparse,
     lmhead_fwd_shard,
     lmhead_get_status,
+    lmhead_get_timeout_record,
     lmhead_launch_count,
     lmhead_merge_shards,
     lmhead_profile_enable,

@@ -1,15 +1,16 @@
-// Instantiations of the tcgen05 GEMMs (one-CTA and CTA-pair) for the kDw
-// contraction; one translation unit per contraction so the four compile in
-// parallel.
+// Instantiations of the tcgen05 GEMMs (one-CTA, and CTA pairs with 256- and
+// 512-column tiles) for the kDw contraction; one translation unit per
+// contraction so the four compile in parallel.
 #include "tc_gemm.cuh"
 #include "tc_gemm2.cuh"
-#include "tc_gemm4.cuh"
 
 namespace lmhead {
 template cudaError_t launch_tc_gemm<kDw>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                           const TcGemmParams&, int, cudaStream_t);
-template cudaError_t launch_tc_gemm_pair<kDw>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                                const TcGemmParams&, int, cudaStream_t);
-template cudaError_t launch_tc_gemm_quad<kDw>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                                const TcGemmParams&, int64_t, cudaStream_t, int*);
+                                       const TcGemmParams&, int, cudaStream_t);
+template cudaError_t launch_tc_gemm_pair<kDw, 1>(const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const TcGemmParams&, int,
+                                               cudaStream_t);
+template cudaError_t launch_tc_gemm_pair<kDw, 2>(const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const TcGemmParams&, int,
+                                               cudaStream_t);
 }  // namespace lmhead

@@ -113,21 +113,15 @@ cudaError_t launch_tc_gemm(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                            const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
                            cudaStream_t stream);
 
-// The same contractions on CTA pairs (256 x 256 tiles, cta_group::2); `grid`
-// must be even.  Its B maps use 128-row boxes (each CTA stages half of B).
-template <int MODE>
+// The same contractions on CTA pairs (cta_group::2, tc_gemm2.cuh): tiles of
+// 256 rows x NSUB * 256 columns (NSUB = 1: two double-buffered 256-column
+// accumulators; NSUB = 2: one 512-column accumulator).  `grid` must be even;
+// the B maps use 128-row boxes for K-major B (each CTA stages half of every
+// 256-column block of B).
+template <int MODE, int NSUB>
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
                                 const CUtensorMap& tma_c, const TcGemmParams& p, int grid,
                                 cudaStream_t stream);
-
-// The same contractions on clusters of two CTA pairs that share A by TMA
-// multicast (tc_gemm4.cuh): `units` = row tiles x column-tile pairs (x the
-// largest dHidden K split); A maps use 64-row boxes (K-major A).  The
-// clusters launched go to *clusters_out (the workers of the split rule).
-template <int MODE>
-cudaError_t launch_tc_gemm_quad(const CUtensorMap& tma_a, const CUtensorMap& tma_b,
-                                const CUtensorMap& tma_c, const TcGemmParams& p, int64_t units,
-                                cudaStream_t stream, int* clusters_out);
 
 // The Nk kept rows are cut into ceil(Nk / C) chunks of equal size rounded up
 // to 256 rows (so no chunk is much shorter than the others and the per-chunk

@@ -22,9 +22,6 @@ namespace {
 constexpr int kDhMaxSplit = 4;  // largest K split of the dHidden contraction
 static_assert(kDhMaxSplit <= 4, "the dHidden reduction sums at most four partials");
 constexpr int kDhSplitFillPct = 85;  // split only when fewer worker slots than this are busy
-// The same threshold for the four-CTA variant, whose 36 workers leave a
-// larger last-wave gap (7.1 waves of 256 units run as 8).
-constexpr int kDhSplitFillPctQuad = 92;
 // Raster blocks of the vocabulary projections (kFwd, kDz): 32 MB of bf16 Hc
 // rows, but never fewer than 4096 rows.  The block stays in L2 (together with
 // the vocabulary tiles in flight) while W streams past once per block; measured
@@ -248,6 +245,13 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 lmhead_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LMHEAD_OK : LMHEAD_ECUDA; }
 
+// Clears the status word and the timeout record of the workspace header
+// (status[0] and status[3]; Nk and the tile count in between are rewritten
+// by every call that reads them).
+cudaError_t clear_status(int* status, cudaStream_t s) {
+  return cudaMemsetAsync(status, 0, 4 * sizeof(int), s);
+}
+
 #define LM_TRY(expr)                                  \
   do {                                                \
     cudaError_t e_ = (expr);                          \
@@ -283,58 +287,75 @@ int gemm_grid(int64_t tiles) {
   return static_cast<int>(tiles < sms ? (tiles < 1 ? 1 : tiles) : sms);
 }
 
-// GEMM variant of one contraction.  By default dHidden runs on clusters of
-// two CTA pairs that share its A operand (the dZ rows) by TMA multicast and
-// the other three on CTA pairs (256 x 256 tiles): on the fwd + bwd step at
-// H = 4096 and 5120 the shared dZ stream saves 1.3%, while sharing the A
-// operand of the projections or of dW saved nothing.  The two pairs of a
-// cluster take neighbouring column tiles, so dHidden stays on CTA pairs when
-// H spans an odd number of 256-column tiles (the last cluster's second pair
-// would have no tile).  LMHEAD_GEMM = "single" (one-CTA kernel, 128 x 256
-// tiles), "pair" or "quad" puts every contraction on one variant.
-// Block-sparse calls never use the four-CTA variant.
-enum class GemmVariant { kSingle, kPair, kQuad };
+// GEMM variant of one contraction.  By default the projections (kFwd, kDz)
+// and dW run on CTA pairs with 256 x 256 tiles and double-buffered
+// accumulators (their K = H or the chunk's rows is short, so the epilogue of
+// one tile must hide behind the MMAs of the next), and dHidden on CTA pairs
+// with 256 x 512 tiles (K = V is long: one 512-column accumulator, a third
+// fewer operand bytes per FLOP and half the passes over W).
+//   LMHEAD_GEMM = "single" (one-CTA kernel, 128 x 256 tiles), "pair" or
+//     "wide" puts every contraction on one variant;
+//   LMHEAD_WIDE = a comma-separated subset of "fwd,dz,dh,dw" replaces the
+//     default set of contractions on 512-column tiles (when LMHEAD_GEMM is
+//     unset; "none" for the empty set).
+enum class GemmVariant { kSingle, kPair, kWide };
 
-GemmVariant gemm_variant(bool blocksparse, int mode, int H) {
+bool listed(const char* list, const char* name) {
+  const size_t n = std::strlen(name);
+  for (const char* p = list; *p != 0;) {
+    const char* e = std::strchr(p, ',');
+    const size_t len = e != nullptr ? static_cast<size_t>(e - p) : std::strlen(p);
+    if (len == n && std::strncmp(p, name, n) == 0) return true;
+    if (e == nullptr) break;
+    p = e + 1;
+  }
+  return false;
+}
+
+GemmVariant gemm_variant(int mode) {
   const char* e = std::getenv("LMHEAD_GEMM");
   if (e != nullptr && std::strcmp(e, "single") == 0) return GemmVariant::kSingle;
   if (e != nullptr && std::strcmp(e, "pair") == 0) return GemmVariant::kPair;
-  const bool quad = e != nullptr && std::strcmp(e, "quad") == 0
-                        ? true
-                        : mode == kDh && cdiv(H, kBN) % 2 == 0;
-  return quad && !blocksparse ? GemmVariant::kQuad : GemmVariant::kPair;
+  if (e != nullptr && std::strcmp(e, "wide") == 0) return GemmVariant::kWide;
+  static const char* kNames[4] = {"fwd", "dz", "dh", "dw"};
+  const char* w = std::getenv("LMHEAD_WIDE");
+  const bool wide = w != nullptr ? listed(w, kNames[mode]) : mode == kDh;
+  return wide ? GemmVariant::kWide : GemmVariant::kPair;
 }
 
-// Rows of one tile of the selected variant.
+// Rows and columns of one tile of the selected variant.
 inline int tile_rows(GemmVariant v) { return v == GemmVariant::kSingle ? kBM : 256; }
+inline int tile_cols(GemmVariant v) { return v == GemmVariant::kWide ? 2 * kBN : kBN; }
+
+// Largest K split of dHidden: LMHEAD_DH_SPLIT = 1 .. 4 (default 4; 1 never
+// splits).
+int dh_max_split() {
+  const char* e = std::getenv("LMHEAD_DH_SPLIT");
+  if (e == nullptr) return kDhMaxSplit;
+  const int v = std::atoi(e);
+  return v < 1 ? 1 : (v > kDhMaxSplit ? kDhMaxSplit : v);
+}
 
 // Launches one contraction on the selected variant.  m_upper bounds the rows
 // of D (the chunk for kFwd/kDz/kDh, V for kDw); b_single / b_pair are the B
-// maps for the two variants (they differ only for K-major B); a_quad is the A
-// map of the quad variant (64-row boxes for K-major A); c is the output map of
-// kDz / kDw (the other contractions do not read it).
-// *workers receives the number of persistent workers launched (CTA pairs or
-// CTAs), which the dHidden split rule depends on.
+// maps for the one-CTA and CTA-pair variants (they differ only for K-major
+// B); c is the output map of kDz / kDw (the other contractions do not read
+// it).  *workers receives the number of persistent workers launched (CTA
+// pairs or CTAs), which the dHidden split rule depends on.
 template <int MODE>
-cudaError_t run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& a_quad,
-                     const CUtensorMap& b_single, const CUtensorMap& b_pair,
-                     const CUtensorMap& c, const TcGemmParams& p, int64_t m_upper, int64_t n,
-                     cudaStream_t s, int* workers = nullptr) {
+cudaError_t run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b_single,
+                     const CUtensorMap& b_pair, const CUtensorMap& c, const TcGemmParams& p,
+                     int64_t m_upper, int64_t n, cudaStream_t s, int* workers = nullptr) {
   if (fault_at("launch")) return cudaErrorLaunchFailure;
   const int split = MODE == kDh ? p.max_split : 1;
-  if (v == GemmVariant::kQuad) {
-    const int64_t units = cdiv(m_upper, 256) * cdiv(cdiv(n, kBN), 2) * split;
-    int clusters = 0;
-    const cudaError_t e = launch_tc_gemm_quad<MODE>(a_quad, b_pair, c, p, units, s, &clusters);
-    if (workers != nullptr) *workers = clusters;
-    return e;
-  }
-  if (v == GemmVariant::kPair) {
-    const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, kBN) * split;
+  if (v == GemmVariant::kPair || v == GemmVariant::kWide) {
+    const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, tile_cols(v)) * split;
     const int64_t pairs = device_info().sms / 2;
     const int64_t w = tiles < pairs ? (tiles < 1 ? 1 : tiles) : pairs;
     if (workers != nullptr) *workers = static_cast<int>(w);
-    return launch_tc_gemm_pair<MODE>(a, b_pair, c, p, static_cast<int>(2 * w), s);
+    return v == GemmVariant::kWide
+               ? launch_tc_gemm_pair<MODE, 2>(a, b_pair, c, p, static_cast<int>(2 * w), s)
+               : launch_tc_gemm_pair<MODE, 1>(a, b_pair, c, p, static_cast<int>(2 * w), s);
   }
   const int grid = gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN) * split);
   if (workers != nullptr) *workers = grid;
@@ -378,7 +399,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   __nv_bfloat16* hc = at<__nv_bfloat16>(workspace, L.hc);
   float4* part = at<float4>(workspace, L.part);
 
-  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  LM_TRY(clear_status(status, s));
   uint8_t* lvalid = blocksparse ? at<uint8_t>(workspace, L.lvalid) : nullptr;
   int32_t* tile_list = at<int32_t>(workspace, L.tlist);
   if (blocksparse) {
@@ -393,11 +414,10 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   }
   if (st != LMHEAD_OK) return st;
 
-  const GemmVariant gv = gemm_variant(blocksparse, kFwd, H);
-  CUtensorMap ma, ma64, mb, mb2;
+  const GemmVariant gv = gemm_variant(kFwd);
+  CUtensorMap ma, mb, mb2;
   if (!(blocksparse ? make_map(&ma, hidden, N, H, H, kBM, 64)
                     : make_map(&ma, hc, L.C, H, H, kBM, 64)) ||
-      !make_map(&ma64, hc, L.C, H, H, 64, 64) ||
       !make_map(&mb, weight, V, H, H, kBN, 64) ||
       !make_map(&mb2, weight, V, H, H, 128, 64))
     return LMHEAD_ECUDA;
@@ -430,7 +450,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
     p.chunk_index = static_cast<int>(c);
     {
       Launch l(kKindGemmFwd, s);
-      LM_TRY(run_gemm<kFwd>(gv, ma, ma64, mb, mb2, ma, p, L.C, V, s));
+      LM_TRY(run_gemm<kFwd>(gv, ma, mb, mb2, ma, p, L.C, V, s));
     }
     {
       Launch l(kKindMerge, s);
@@ -494,7 +514,7 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   __nv_bfloat16* hc = at<__nv_bfloat16>(workspace, L.hc);
   __nv_bfloat16* dz = at<__nv_bfloat16>(workspace, L.dz);
 
-  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  LM_TRY(clear_status(status, s));
   uint8_t* lvalid = blocksparse ? at<uint8_t>(workspace, L.lvalid) : nullptr;
   int32_t* tile_list = at<int32_t>(workspace, L.tlist);
   if (blocksparse) {
@@ -518,11 +538,10 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     LM_TRY(launch_zero_skipped_rows(keep, N, H, static_cast<__nv_bfloat16*>(dhidden), s));
   }
 
-  const GemmVariant gv_dz = gemm_variant(blocksparse, kDz, H);
-  const GemmVariant gv_dh = gemm_variant(blocksparse, kDh, H);
-  const GemmVariant gv_dw = gemm_variant(blocksparse, kDw, H);
-  CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn, m_dz_out, m_dw_out,
-      m_hc_k64, m_dz_k64;
+  const GemmVariant gv_dz = gemm_variant(kDz);
+  const GemmVariant gv_dh = gemm_variant(kDh);
+  const GemmVariant gv_dw = gemm_variant(kDw);
+  CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn, m_dz_out, m_dw_out;
   const void* rows_src = blocksparse ? hidden : static_cast<const void*>(hc);
   const int64_t rows_n = blocksparse ? N : L.C;
   if (!make_map(&m_hc_k, rows_src, rows_n, H, H, kBM, 64) ||  // A of kDz (K-major)
@@ -532,8 +551,6 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       !make_map(&m_w_mn, weight, V, H, H, 64, 64) ||       // B of kDh (MN-major boxes)
       !make_map(&m_dz_mn, dz, L.C, V, L.dz_ld, 64, 64) ||  // A of kDw (MN-major boxes)
       !make_map(&m_hc_mn, rows_src, rows_n, H, H, 64, 64) ||  // B of kDw (MN-major boxes)
-      !make_map(&m_hc_k64, hc, L.C, H, H, 64, 64) ||          // A of kDz, quad variant
-      !make_map(&m_dz_k64, dz, L.C, V, L.dz_ld, 64, 64) ||     // A of kDh, quad variant
       !make_map(&m_dz_out, dz, L.C, V, L.dz_ld, 32, 64) ||   // output of kDz
       !make_map(&m_dw_out, dweight, V, H, H, 32, 32, true))   // output of kDw (fp32)
     return LMHEAD_ECUDA;
@@ -557,10 +574,9 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
   p.want_entropy = grad_entropy ? 1 : 0;
   p.dhidden = static_cast<__nv_bfloat16*>(dhidden);
   p.dh_part = at<float>(workspace, L.dhp);
-  p.max_split = kDhMaxSplit;
-  p.split_fill_pct = gv_dh == GemmVariant::kQuad ? kDhSplitFillPctQuad : kDhSplitFillPct;
+  p.max_split = dh_max_split();
+  p.split_fill_pct = kDhSplitFillPct;
   int dh_workers = 0;
-  const int64_t n_h_tiles = cdiv(H, kBN);
 
   const int64_t max_chunks = cdiv(N, L.C);
   for (int64_t c = 0; c < max_chunks; ++c) {
@@ -576,19 +592,18 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
       Launch l(kKindGemmDz, s);
       p.group_m = row_block_tiles(H, tile_rows(gv_dz), L.C);
       p.group_n = 16;
-      LM_TRY(run_gemm<kDz>(gv_dz, m_hc_k, m_hc_k64, m_w_k, m_w_k2, m_dz_out, p, L.C, V, s));
+      LM_TRY(run_gemm<kDz>(gv_dz, m_hc_k, m_w_k, m_w_k2, m_dz_out, p, L.C, V, s));
     }
     {
       Launch l(kKindGemmDh, s);
       p.group_m = 0;
-      p.group_n = static_cast<int>(n_h_tiles);
-      LM_TRY(run_gemm<kDh>(gv_dh, m_dz_k, m_dz_k64, m_w_mn, m_w_mn, m_dz_k, p, L.C, H, s,
-                           &dh_workers));
+      p.group_n = static_cast<int>(cdiv(H, tile_cols(gv_dh)));  // all column tiles per row tile
+      LM_TRY(run_gemm<kDh>(gv_dh, m_dz_k, m_w_mn, m_w_mn, m_dz_k, p, L.C, H, s, &dh_workers));
     }
     {
       Launch l(kKindDhReduce, s);
       LM_TRY(launch_dh_reduce(p.dh_part, d_nk, static_cast<int>(c), static_cast<int>(L.C), H,
-                              tile_rows(gv_dh), gv_dh == GemmVariant::kQuad ? 2 * kBN : kBN,
+                              tile_rows(gv_dh), tile_cols(gv_dh),
                               dh_workers, static_cast<int>(cdiv(V, kBK)),
                               p.max_split, p.split_fill_pct, idx, lvalid,
                               static_cast<__nv_bfloat16*>(dhidden), N, status, s));
@@ -596,9 +611,9 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     {
       Launch l(kKindGemmDw, s);
       p.group_m = 0;
-      p.group_n = static_cast<int>(n_h_tiles);
+      p.group_n = static_cast<int>(cdiv(H, tile_cols(gv_dw)));  // all column tiles per row tile
       p.beta = (c > 0 || dw_accumulate) ? 1 : 0;
-      LM_TRY(run_gemm<kDw>(gv_dw, m_dz_mn, m_dz_mn, m_hc_mn, m_hc_mn, m_dw_out, p, V, H, s));
+      LM_TRY(run_gemm<kDw>(gv_dw, m_dz_mn, m_hc_mn, m_hc_mn, m_dw_out, p, V, H, s));
     }
   }
   return LMHEAD_OK;
@@ -649,7 +664,7 @@ lmhead_status lmhead_compact(const uint8_t* keep, const int64_t* targets, int64_
   LM_CHECK_PTRS(keep, targets, idx, targets_c, d_nk, workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = at<int>(workspace, L.hdr);
-  LM_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  LM_TRY(clear_status(status, s));
   return run_compact(keep, targets, N, V, 0, idx, targets_c, d_nk,
                      at<int32_t>(workspace, L.counts), status, s);
 }
@@ -806,6 +821,17 @@ lmhead_status lmhead_get_status(const void* workspace, lmhead_stream_t stream) {
   if (cudaMemcpy(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return LMHEAD_ECUDA;
   return static_cast<lmhead_status>(h);
+}
+
+int32_t lmhead_get_timeout_record(const void* workspace, lmhead_stream_t stream) {
+  if (workspace == nullptr) return -1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, static_cast<const int32_t*>(workspace) + 3, sizeof(int32_t),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -1;
+  return h;
 }
 
 const char* lmhead_strerror(lmhead_status status) {

@@ -15,6 +15,24 @@ constexpr int kStatusTarget = 3;    // == LMHEAD_ETARGET
 constexpr int kStatusBounds = 7;    // == LMHEAD_EBOUNDS
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
 
+// Where a pipeline wait ran out.  The first wait of a call that gives up
+// records (site << 24) | blockIdx.x in status[3], the fourth word of the
+// workspace header (status[1] holds Nk, status[2] the active-tile count), so
+// a timeout names its role, its barrier and its CTA.
+enum WaitSite : int {
+  kSiteProducerEmpty = 1,   // producer waiting for a free stage
+  kSiteIssuerTmemEmpty = 2, // MMA issuer waiting for a released accumulator
+  kSiteIssuerFull = 3,      // MMA issuer waiting for a filled stage
+  kSiteEpilogueFull = 4,    // epilogue waiting for a finished accumulator
+  kSiteProducerDrain = 5,   // producer letting its last loads land
+  kSiteIssuerDrain = 6,     // MMA issuer letting its last MMAs finish
+};
+
+__device__ __forceinline__ void record_timeout(int* status, int site) {
+  atomicCAS(status, 0, kStatusTimeout);
+  atomicCAS(status + 3, 0, (site << 24) | static_cast<int>(blockIdx.x & 0xFFFFFFu));
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -71,9 +89,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase of `bar` with the given parity.  Returns false
 // (and leaves the pipeline to be torn down) if another role aborted or if the
 // wait exceeded kWaitLimitNs, in which case the device status becomes
-// ETIMEOUT.
+// ETIMEOUT and `site` is recorded (record_timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   uint32_t n = 0;
@@ -83,7 +101,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       if (*abort_flag) return false;
       if (global_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
-        atomicCAS(status, 0, kStatusTimeout);
+        record_timeout(status, site);
         return false;
       }
     }
@@ -280,19 +298,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y)
-      : "memory");
-}
-
-// The same load multicast to the CTAs of `cta_mask` (same shared-memory
-// offset in each); the completion of the bytes landing in a CTA is counted on
-// the barrier at bar_cluster_addr's offset in the even CTA of that CTA's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map,
-                                                    uint32_t bar_cluster_addr, int x, int y,
-                                                    uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask)
       : "memory");
 }
 

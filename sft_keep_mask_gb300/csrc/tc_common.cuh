@@ -63,11 +63,12 @@ __host__ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n
 // Wait without the abort check: used only to drain copies / MMAs in flight
 // before the CTA releases its shared and tensor memory.  Running out of time
 // here is recorded like any other timeout.
-__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status,
+                                                int site) {
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_ns() - t0 > kWaitLimitNs) {
-      atomicCAS(status, 0, kStatusTimeout);
+      record_timeout(status, site);
       return;
     }
   }

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tile_coords(t, num_m, num_n, p.group_m, p.group_n, mt, nt);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kSiteProducerEmpty)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * kBBytes;
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // Let every load that was issued land before the CTA exits.
       for (int s = 0; s < kStages; ++s) {
         const uint32_t uses = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
-        if (uses > 0) mbar_wait_drain(&full[s], (uses - 1u) & 1u, p.status);
+        if (uses > 0) mbar_wait_drain(&full[s], (uses - 1u) & 1u, p.status, kSiteProducerDrain);
       }
     }
     __syncwarp();
@@ -164,11 +164,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
-        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status, kSiteIssuerTmemEmpty))
+          break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kSiteIssuerFull)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_addr(sA + stage * kABytes);
           const uint32_t b_addr = smem_addr(sB + stage * kBBytes);
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // No MMA may still be running when the accumulators are released.
       umma_commit(drain);
-      mbar_wait_drain(drain, 0, p.status);
+      mbar_wait_drain(drain, 0, p.status, kSiteIssuerDrain);
     }
     __syncwarp();
   } else {
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       if (num_kb > 0) {
-        if (!mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status)) break;
+        if (!mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status, kSiteEpilogueFull)) break;
         tc_fence_after();
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);

@@ -63,6 +63,7 @@ _SIGS = {
     "lmhead_selective_log_softmax_bwd": (_I32, [_VP, _I32, _I64, _VP, _VP, _I64, _I32, _VP, _VP,
                                                 _VP, _VP, _VP, _I64, _VP, _VP]),
     "lmhead_get_status": (_I32, [_VP, _VP]),
+    "lmhead_get_timeout_record": (ctypes.c_int32, [_VP, _VP]),
     "lmhead_workspace_kept_rows": (_VP, [_VP]),
     "lmhead_strerror": (ctypes.c_char_p, [_I32]),
     "lmhead_profile_enable": (None, [_I32]),
@@ -365,6 +366,21 @@ def lmhead_selective_log_softmax_bwd(logits, targets, keep, lse, entropy, grad_l
 def lmhead_get_status(workspace, stream=None) -> int:
     """Device status of the last call on this workspace (synchronises)."""
     return int(_call("lmhead_get_status", (workspace,), _p(workspace), stream=stream))
+
+
+# Pipeline waits named by lmhead_get_timeout_record (site codes 1 .. 6).
+TIMEOUT_SITES = {1: "producer: free stage", 2: "MMA issuer: released accumulator",
+                 3: "MMA issuer: filled stage", 4: "epilogue: finished accumulator",
+                 5: "producer: drain of its loads", 6: "MMA issuer: drain of its MMAs"}
+
+
+def lmhead_get_timeout_record(workspace, stream=None):
+    """(site, cta) of the first pipeline wait that gave up in the last call on
+    this workspace, or None if none did (synchronises)."""
+    rec = int(_call("lmhead_get_timeout_record", (workspace,), _p(workspace), stream=stream))
+    if rec < 0:
+        raise LmheadError(LMHEAD_ECUDA, "lmhead_get_timeout_record")
+    return None if rec == 0 else (rec >> 24, rec & 0xFFFFFF)
 
 
 def lmhead_workspace_kept_rows(workspace):

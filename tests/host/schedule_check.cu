@@ -4,10 +4,12 @@
 //   * chunk_span splits Nk kept rows into chunks that cover [0, Nk) in order,
 //     each at most chunk_rows long;
 //   * dh_split_count never splits past the K blocks or the partial buffers;
-//   * the four-CTA kernel's units (a row tile x a pair of column tiles x a K
-//     part) cover every (row tile, column tile, K part) once, the K parts
-//     partition the K blocks, and dh_reduce_kernel, which counts units as
-//     row tiles x ceil(H / 512), sees the same unit count as the kernel.
+//   * the 512-column tiles of the CTA-pair kernel, walked as the kernel walks
+//     them (raster over wide tiles, then their two 256-column blocks), cover
+//     every (row tile, 256-column tile, K part) once -- a block past the last
+//     256-column tile only when that count is odd -- and the K parts
+//     partition the K blocks; dh_reduce_kernel, which counts the tiles as
+//     row tiles x ceil(H / 512), sees the kernel's unit count.
 // Prints "ok" and exits 0, or names the first failing case and exits 1.
 #include <cstdio>
 #include <vector>
@@ -35,36 +37,36 @@ static int check_raster(int num_m, int num_n, int group_m, int group_n) {
   return 0;
 }
 
-// Units of the four-CTA kernel, walked as the kernel walks them.
-static int check_quad_units(int num_m, int num_n, int group_m, int group_n, int splits,
+// Units of the CTA-pair kernel with 512-column tiles, walked as it walks them.
+static int check_wide_units(int num_m, int num_n, int group_m, int group_n, int splits,
                             int num_kb) {
-  const int num_np = (num_n + 1) / 2;
-  const int num_base = num_m * num_np;
+  const int num_nw = (num_n + 1) / 2;   // 512-column tiles over num_n 256-column tiles
+  const int num_tiles = num_m * num_nw;
   std::vector<int> seen(static_cast<size_t>(num_m) * num_n * splits, 0);
   std::vector<int> kcover(static_cast<size_t>(num_kb), 0);
-  for (int u = 0; u < num_base * splits; ++u) {
-    const int sidx = u / num_base;
+  for (int u = 0; u < num_tiles * splits; ++u) {
+    const int sidx = u / num_tiles;
     const int kb0 = static_cast<int>(static_cast<long long>(sidx) * num_kb / splits);
     const int kb1 = static_cast<int>(static_cast<long long>(sidx + 1) * num_kb / splits);
     if (kb1 <= kb0) {
-      std::printf("quad: empty K part %d of %d over %d blocks\n", sidx, splits, num_kb);
+      std::printf("wide: empty K part %d of %d over %d blocks\n", sidx, splits, num_kb);
       return 1;
     }
-    int mt = -1, ntp = -1;
-    tile_coords(u % num_base, num_m, num_np, group_m, group_n, mt, ntp);
-    if (u % num_base == 0)
+    int mt = -1, ntw = -1;
+    tile_coords(u % num_tiles, num_m, num_nw, group_m, group_n, mt, ntw);
+    if (u % num_tiles == 0)
       for (int kb = kb0; kb < kb1; ++kb) ++kcover[static_cast<size_t>(kb)];
-    for (int pq = 0; pq < 2; ++pq) {
-      const int nt = 2 * ntp + pq;
+    for (int h = 0; h < 2; ++h) {
+      const int nt = 2 * ntw + h;
       if (nt >= num_n) {
-        if (pq == 0 || nt > num_n) {  // only the odd last column tile may be missing
-          std::printf("quad: unit %d -> column tile %d of %d\n", u, nt, num_n);
+        if (h == 0 || nt > num_n) {  // only the odd last block may lie past the grid
+          std::printf("wide: unit %d -> column tile %d of %d\n", u, nt, num_n);
           return 1;
         }
         continue;
       }
       if (mt < 0 || mt >= num_m || seen[(static_cast<size_t>(sidx) * num_m + mt) * num_n + nt]++) {
-        std::printf("quad: M=%d N=%d gm=%d gn=%d S=%d unit %d repeats or leaves the grid\n",
+        std::printf("wide: M=%d N=%d gm=%d gn=%d S=%d unit %d repeats or leaves the grid\n",
                     num_m, num_n, group_m, group_n, splits, u);
         return 1;
       }
@@ -72,13 +74,13 @@ static int check_quad_units(int num_m, int num_n, int group_m, int group_n, int 
   }
   for (int v : seen)
     if (v != 1) {
-      std::printf("quad: M=%d N=%d gm=%d gn=%d S=%d misses a tile\n", num_m, num_n, group_m,
+      std::printf("wide: M=%d N=%d gm=%d gn=%d S=%d misses a tile\n", num_m, num_n, group_m,
                   group_n, splits);
       return 1;
     }
   for (int v : kcover)
     if (v != 1) {
-      std::printf("quad: K parts of %d blocks in %d parts do not partition\n", num_kb, splits);
+      std::printf("wide: K parts of %d blocks in %d parts do not partition\n", num_kb, splits);
       return 1;
     }
   return 0;
@@ -132,14 +134,14 @@ int main() {
         for (int gn : {1, 4, 16})
           for (int s : {1, 2, 3, 4})
             for (int kb : {4, 7, 2374})
-              if (check_quad_units(m, n, gm, gn, s, kb)) return 1;
+              if (check_wide_units(m, n, gm, gn, s, kb)) return 1;
 
-  // dh_reduce_kernel's unit count (tile_m = 256, tile_n = 512) equals the
-  // four-CTA kernel's for every H, so both take the same K split
+  // dh_reduce_kernel's tile count (tile_m = 256, tile_n = 512) equals the
+  // wide kernel's for every H, so both take the same K split
   for (int H = 8; H <= 16384; H += 8) {
     const int num_n = (H + kBN - 1) / kBN;
     if ((num_n + 1) / 2 != (H + 2 * kBN - 1) / (2 * kBN)) {
-      std::printf("quad unit count differs from the reduction's at H=%d\n", H);
+      std::printf("wide tile count differs from the reduction's at H=%d\n", H);
       return 1;
     }
   }

@@ -1,10 +1,10 @@
 """The GPU parity suites again with every contraction on one GEMM variant.
 
-By default dHidden runs on the four-CTA kernel (two CTA pairs sharing the dZ
-rows by TMA multicast) and the other contractions on CTA pairs.
-LMHEAD_GEMM=single, =pair or =quad puts all four contractions on the
-one-CTA (128 x 256 tiles), CTA-pair or four-CTA kernel; they share the
-epilogues and must give the same results.  A few parity tests pick a variant
+By default dHidden runs on CTA pairs with 256 x 512 tiles and the other
+contractions on CTA pairs with 256 x 256 tiles.  LMHEAD_GEMM=single, =pair or
+=wide puts all four contractions on the one-CTA (128 x 256 tiles), CTA-pair
+(256 x 256) or wide CTA-pair (256 x 512) kernel; they share the epilogues and
+must give the same results.  A few parity tests pick a variant
 directly; here the parity, shard and autograd suites run in a child process
 with each variant selected (tests that pick a variant themselves keep their
 choice).
@@ -21,7 +21,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITE = ["tests/test_gpu_parity.py", "tests/test_gpu_shards.py", "tests/test_gpu_autograd.py"]
 
 
-@pytest.mark.parametrize("variant", ["single", "pair", "quad"])
+@pytest.mark.parametrize("variant", ["single", "pair", "wide"])
 def test_parity_suites_pass_on_one_variant(variant):
     env = dict(os.environ, LMHEAD_GEMM=variant)
     r = subprocess.run([sys.executable, "-m", "pytest", *SUITE, "-m", "gpu", "-x", "-q",

@@ -4,8 +4,9 @@
 (tile raster, chunk spans, dHidden K-split rule) and runs them on the CPU:
 every tile index must map to a distinct tile of the grid, the chunks must
 cover the kept rows in order, the split count must stay within bounds, and
-the four-CTA kernel's units (row tile x column-tile pair x K part) must cover
-every tile and K block once, counted as the dHidden reduction counts them.
+the 512-column tiles of the CTA-pair kernel (row tile x two 256-column
+blocks x K part) must cover every tile and K block once, counted as the
+dHidden reduction counts them.
 """
 
 import os
