@@ -7,9 +7,15 @@ expansion; then the backward: compaction, logit recomputation with the dZ
 epilogue, dHidden (scattered back) and dW contractions per chunk.
 
 Default workload: 30B-MoE-shaped RL head, N=65536 packed tokens, H=4096,
-V=151936, bf16, sequences of length ~U[512, 8192] with a prompt fraction
-~U[0.3, 0.7] masked (about half the rows kept), differentiable entropy
-(grad_entropy = -0.01).
+V=151936, bf16, sequences of length ~U[512, 8192] whose first half (prompt
+fraction 0.5) is masked, so half the rows are kept (32767 of 65536),
+differentiable entropy (grad_entropy = -0.01).  `--workload moe30b_rl` draws
+the prompt fraction ~U[0.3, 0.7] instead (55% kept).
+
+With --gpus N > 1 the step runs data-parallel on N ranks (one process per
+GPU, under torch.distributed.run; started by this script when it is run
+without one): every rank scores its own batch and the weight gradients are
+summed by one all-reduce after the backward, inside the timed region.
 
 Prints one JSON line.  `--impl reference` times the float64 CPU oracle on a
 bounded sample of kept rows of the same workload instead.
@@ -77,6 +83,34 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def launch_plan(gpus, env):
+    """What `--gpus N` asks for, given the environment: "run" (this process
+    is one of the N ranks, or N == 1), "spawn" (no launcher: start N ranks
+    under torch.distributed.run) or an error message (a launcher started a
+    different number of ranks)."""
+    if gpus < 1:
+        return f"--gpus must be at least 1, got {gpus}"
+    if "WORLD_SIZE" not in env:
+        return "run" if gpus == 1 else "spawn"
+    world = int(env["WORLD_SIZE"])
+    if world != gpus:
+        return f"--gpus {gpus} but the launcher started {world} ranks"
+    return "run"
+
+
+def spawn_ranks(gpus, argv):
+    """Re-runs this script as `gpus` ranks on this node (torch.distributed.run,
+    rendezvous on 127.0.0.1) and returns its exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={gpus}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
 
 
 class ClockSampler:
@@ -189,7 +223,7 @@ def run_config(args, N, H, V, nk, world, entropy_grad):
             "rows": "block-sparse tiles" if args.blocksparse else "compacted",
             "l2": ("inputs larger than L2" if big else "inputs fit in L2 (no flush)")
                   + f" (W {w_bytes / 1e9:.2f} GB, hidden {h_bytes / 1e9:.2f} GB)",
-            "parallelism": f"replicas x{world}"}
+            "parallelism": f"dp{world}" if world > 1 else "single GPU"}
 
 
 def entropy_grad_of(args, inp):
@@ -213,8 +247,9 @@ def _workload(args):
 def reduce_over_ranks(elapsed, kept, world, device):
     """(max elapsed over ranks, sum of kept rows over ranks).
 
-    Every rank scores its own batch (replicas, weak scaling), so the job's
-    time is the slowest rank's and its work is the sum of all ranks' rows.
+    Every rank scores its own batch (data-parallel, weak scaling), so the
+    job's time is the slowest rank's and its work is the sum of all ranks'
+    rows.
     """
     if world <= 1:
         return float(elapsed), float(kept)
@@ -286,7 +321,7 @@ def run_ours(args):
     import torch
     from sft_keep_mask_gb300 import lmhead as L
     from sft_keep_mask_gb300 import synth
-    from sft_keep_mask_gb300.api import LMHeadScorer
+    from sft_keep_mask_gb300.api import LMHeadScorer, allreduce_weight_grad
 
     world, rank, local = _dist()
     if world > 1:
@@ -339,6 +374,8 @@ def run_ours(args):
         if args.mode == "fwdbwd":
             bwd(hidden, inp["weight"], targets, keep_arg, lse, ent, g_lp, g_e, dh, dW, False, ws,
                 args.chunk_rows, stream)
+            # data-parallel ranks: one all-reduce of dW after the backward
+            allreduce_weight_grad(dW)
 
     loss_mask = comps[0] if comps is not None else None
     dev_args = (inp["hidden"], inp["targets"], loss_mask, offsets, inp["grad_logprob"], g_ent)
@@ -347,7 +384,8 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     status = L.lmhead_get_status(ws)
     if status != 0:
-        raise RuntimeError(f"device status {status} after warm-up")
+        raise RuntimeError(f"device status {status} after warm-up "
+                           f"(timeout record {L.lmhead_get_timeout_record(ws)})")
     nk = N if args.keep_off else int(keep.sum().item())
 
     # ---------------------------------------------------------- device-timed
@@ -381,7 +419,8 @@ def run_ours(args):
     launches = L.lmhead_launch_count() - launches0
     status_timed = L.lmhead_get_status(ws)
     if status_timed != 0:
-        raise RuntimeError(f"device status {status_timed} after the timed steps")
+        raise RuntimeError(f"device status {status_timed} after the timed steps "
+                           f"(timeout record {L.lmhead_get_timeout_record(ws)})")
     prof = L.lmhead_profile_read()
     ms = ev0.elapsed_time(ev1)
     ms_max, nk_total = reduce_over_ranks(ms, nk, world, dev)
@@ -440,7 +479,10 @@ def run_ours(args):
         if L.lmhead_get_status(ws) != 0:
             raise RuntimeError("device status non-zero after the end-to-end steps")
         e2e = {"value": nk_total * args.steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * el / args.steps}
+               "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * el / args.steps,
+               "copies": "in: hidden, targets, loss mask, sequence offsets, grad_logprob, "
+                         "grad_entropy; out: logprob and entropy. dhidden and dW stay on the "
+                         "device (they feed the caller's backward and optimizer)"}
 
     # ---------------------------------------------------------- CPU oracle
     cpu = None
@@ -560,7 +602,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="moe30b_rl")
+    ap.add_argument("--workload", default="moe30b_rl_half")
     ap.add_argument("--chunk-rows", type=int, default=0)
     ap.add_argument("--rows", type=int, default=0, help="override N (profiling cases)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling cases)")
@@ -581,6 +623,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    plan = launch_plan(args.gpus, os.environ)
+    if plan == "spawn":
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
+    if plan != "run":
+        print(plan, file=sys.stderr)
+        sys.exit(2)
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "selective_log_softmax":

@@ -155,3 +155,19 @@ class StepPipeline:
             pending = self.done[slot]
         pending.synchronize()
         return self.host_results[(len(batches) - 1) % 2]
+
+
+def allreduce_weight_grad(dweight, group=None):
+    """Data-parallel sum of the weight gradient over the ranks of `group`.
+
+    Rows are independent for logprob, entropy and dhidden, so data-parallel
+    ranks score their own batches; the weight gradient is the one exchange:
+    one all-reduce after the backward (SkyRL pull request #2374, gemini review:
+    a single reduction after the loop, not one per chunk).  This is the
+    caller's collective (torch.distributed: NCCL between GPUs, gloo on CPU
+    tensors), issued on the current stream; with one rank it does nothing.
+    """
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(dweight, op=dist.ReduceOp.SUM, group=group)
+    return dweight

@@ -11,7 +11,11 @@ Workloads (seed = workload number):
                      two packed sequences of 8192, 40% prompt / 60% completion.
 3. ``moe30b_rl``     N=65536, H=4096, V=151936; sequences of length
                      ~U[512, 8192] packed to exactly N, prompt fraction
-                     ~U[0.3, 0.7] masked (about half the rows kept).
+                     ~U[0.3, 0.7] masked (55% of the rows kept in the seed-3
+                     draw).
+   ``moe30b_rl_half`` the same packed sequences with the prompt fraction
+                     exactly 0.5 (the first half of every sequence masked):
+                     half the rows kept (49.98%) whatever the seed.
 4. ``entropy_bonus`` N=16384, H=4096, V=131072; 16 sequences of 1024 whose
                      last round(f * 1024) tokens are active, f a parameter.
 5. ``long_context``  N=262144, H=5120, V=151936; alternating prompt spans
@@ -41,12 +45,15 @@ class Workload:
     mask: str = "bernoulli"          # bernoulli | two_seq | packed | suffix | alternating
     grad_entropy: str = "normal"     # normal | const | none
     want_entropy: bool = True
+    prompt_frac: tuple = (0.3, 0.7)  # packed: bounds of the uniform prompt fraction
 
 
 WORKLOADS = {
     "tiny": Workload("tiny", 1, 256, 256, 4096, 1.0, "bernoulli", "normal"),
     "qwen3_4b": Workload("qwen3_4b", 2, 16384, 2560, 151936, 4.0, "two_seq", "none"),
     "moe30b_rl": Workload("moe30b_rl", 3, 65536, 4096, 151936, 1.0, "packed", "const"),
+    "moe30b_rl_half": Workload("moe30b_rl_half", 3, 65536, 4096, 151936, 1.0, "packed", "const",
+                               prompt_frac=(0.5, 0.5)),
     "entropy_bonus": Workload("entropy_bonus", 4, 16384, 4096, 131072, 1.0, "suffix", "const"),
     "long_context": Workload("long_context", 5, 262144, 5120, 151936, 1.0, "alternating", "const"),
 }
@@ -74,7 +81,7 @@ def _spans(rng: np.random.Generator, w: Workload, active_frac: float):
         while pos < n:
             length = int(rng.integers(512, 8193))
             length = min(length, n - pos)
-            frac = float(rng.uniform(0.3, 0.7))
+            frac = float(rng.uniform(*w.prompt_frac))
             p = int(round(frac * length))
             mask[pos + p:pos + length] = 1.0
             lens.append(length)

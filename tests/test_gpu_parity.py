@@ -234,6 +234,93 @@ def test_full_size_qwen3_4b_forward_sampled():
     _sampled_rows_check(w, inp, keep, dict(lp=lp, ent=ent, lse=lse), 48, False)
 
 
+def test_full_size_qwen3_4b_forward_backward_metric_only_sampled():
+    # the Qwen3-4B head's fwd + bwd with the entropy as a metric only (no
+    # entropy gradient, [P2] How it works): sampled rows against the oracle
+    w = synth.workload("qwen3_4b")
+    inp = synth.make_inputs(w, device=DEV)
+    assert inp["grad_entropy"] is None
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    keep = gpu_keep(sc, inp)
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+    dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                         inp["grad_logprob"], None)
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    _sampled_rows_check(w, inp, keep, dict(lp=lp, ent=ent, lse=lse, dh=dh), 32, True)
+    k = keep.bool()
+    assert (dh[~k] == 0).all() and (lp[~k] == 0).all()
+    col = dW.double().sum(0)
+    assert col.abs().max().item() <= 1e-3 * dW.double().abs().sum(0).max().item()
+
+
+def test_full_size_half_kept_forward_backward_sampled():
+    # the bench's workload: 64K packed tokens, half of them kept
+    w = synth.workload("moe30b_rl_half")
+    inp = synth.make_inputs(w, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V)
+    keep = gpu_keep(sc, inp)
+    np.testing.assert_array_equal(keep.cpu().numpy(), oracle_keep(inp))
+    assert int(keep.sum().item()) == 32767
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+    dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                         inp["grad_logprob"], inp["grad_entropy"])
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    _sampled_rows_check(w, inp, keep, dict(lp=lp, ent=ent, lse=lse, dh=dh), 24, True)
+    k = keep.bool()
+    assert (dh[~k] == 0).all()
+    col = dW.double().sum(0)
+    assert col.abs().max().item() <= 1e-3 * dW.double().abs().sum(0).max().item()
+
+
+_DEPTH = {}
+
+
+def _full_depth_case():
+    """8192 kept rows of 9000 at H = 4096 and V = 3000, with the oracle's
+    whole dhidden and dW (computed once for the variants that reuse it)."""
+    if not _DEPTH:
+        w = synth.workload("moe30b_rl", seed=33, N=9000, V=3000)
+        inp = synth.make_inputs(w, device=DEV)
+        keep_np = np.zeros(w.N, np.uint8)
+        keep_np[np.random.default_rng(33).choice(w.N, 8192, replace=False)] = 1
+        odh, odW = O.backward(to64(inp["hidden"]), to64(inp["weight"]),
+                              inp["targets"].cpu().numpy(), keep_np,
+                              inp["grad_logprob"].cpu().double().numpy(),
+                              inp["grad_entropy"].cpu().double().numpy())
+        _DEPTH.update(w=w, inp=inp, keep_np=keep_np, odh=odh, odW=odW)
+    return _DEPTH
+
+
+@pytest.mark.parametrize("variant", ["pair", "single", "wide"])
+def test_weight_gradient_at_full_chunk_depth(monkeypatch, variant):
+    # one chunk of 8192 kept rows: the dW contraction runs over K = 8192 (128
+    # K blocks, deeper than a default-bench chunk) for all 16 column tiles of
+    # H = 4096; the whole dW is compared element-wise, written and
+    # accumulated onto a prior gradient
+    monkeypatch.setenv("LMHEAD_GEMM", variant)
+    c = _full_depth_case()
+    w, inp, keep_np = c["w"], c["inp"], c["keep_np"]
+    keep = torch.from_numpy(keep_np).to(DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=8192)
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+    g = (inp["grad_logprob"], inp["grad_entropy"])
+    dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent, *g)
+    prior = torch.randn(w.V, w.H, generator=torch.Generator(device=DEV).manual_seed(5),
+                        device=DEV)
+    acc = prior.clone()
+    sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent, *g, dweight=acc,
+                accumulate=True)
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    assert int(sc.kept_rows().item()) == 8192
+    assert_frob_close(dW.cpu().double().numpy(), c["odW"], "dW (K = 8192)")
+    assert_frob_close((acc.double() - prior.double()).cpu().numpy(), c["odW"],
+                      "accumulated dW (K = 8192)")
+    assert_frob_close(to64(dh), c["odh"], "dhidden (K = 8192)")
+
+
 def test_full_size_moe30b_rl_forward_backward_sampled():
     w = synth.workload("moe30b_rl")
     inp = synth.make_inputs(w, device=DEV)
@@ -293,7 +380,7 @@ def test_variants_agree_bitwise(monkeypatch):
     w = synth.workload("tiny", seed=21, N=900, H=320, V=3000)
     inp = synth.make_inputs(w, device=DEV)
     res = []
-    for variant in ("pair", "single", "quad"):
+    for variant in ("pair", "single", "wide"):
         monkeypatch.setenv("LMHEAD_GEMM", variant)  # the previous value comes back after the test
         sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
         lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], inp["keep"])
@@ -316,7 +403,7 @@ def test_chunk_boundaries(nk):
     _run_both(w, keep_override=keep, chunk_rows=256)
 
 
-@pytest.mark.parametrize("variant", ["pair", "single", "quad"])
+@pytest.mark.parametrize("variant", ["pair", "single", "wide"])
 @pytest.mark.parametrize("N,H,V", [(1, 8, 1), (5, 16, 2), (33, 64, 7), (300, 8, 300),
                                    (70, 24, 129)])
 def test_tiny_and_degenerate_shapes(monkeypatch, variant, N, H, V):
@@ -333,7 +420,7 @@ def test_tiny_and_degenerate_shapes(monkeypatch, variant, N, H, V):
 
 # ------------------------------------------------ block-sparse tile skipping
 
-@pytest.mark.parametrize("variant", ["pair", "single"])
+@pytest.mark.parametrize("variant", ["pair", "single", "wide"])
 def test_blocksparse_matches_the_oracle(monkeypatch, variant):
     monkeypatch.setenv("LMHEAD_GEMM", variant)
     # contiguous active suffixes (the entropy-bonus layout), ragged H and V,
@@ -424,7 +511,7 @@ def test_random_shape_sweep(monkeypatch):
         chunk = int(rng.choice([0, 256, 512, 768]))
         density = float(rng.choice([0.0, 0.05, 0.5, 1.0]))
         keep = (rng.random(N) < density).astype(np.uint8)
-        variant = str(rng.choice(["pair", "single", "quad"]))
+        variant = str(rng.choice(["pair", "single", "wide"]))
         bs = bool(rng.integers(0, 2))
         ent = bool(rng.integers(0, 2))
         monkeypatch.setenv("LMHEAD_GEMM", variant)  # restored after the test
@@ -432,7 +519,7 @@ def test_random_shape_sweep(monkeypatch):
         _run_both(w, chunk_rows=chunk, keep_override=keep, blocksparse=bs, grad_entropy=ent)
 
 
-@pytest.mark.parametrize("variant", ["pair", "single", "quad"])
+@pytest.mark.parametrize("variant", ["pair", "single", "wide"])
 def test_wide_hidden_and_long_vocabulary(monkeypatch, variant):
     # H = 8192: 128 K steps in the projections and 32 column tiles in dHidden
     # and dW; V = 200000: 782 vocabulary tiles ending in a 64-wide tail, so
@@ -443,7 +530,7 @@ def test_wide_hidden_and_long_vocabulary(monkeypatch, variant):
     _run_both(synth.workload("tiny", seed=511, N=96, H=256, V=200000), chunk_rows=256)
 
 
-@pytest.mark.parametrize("variant", ["pair", "single", "quad"])
+@pytest.mark.parametrize("variant", ["pair", "single", "wide"])
 def test_widest_hidden_and_largest_vocabulary(monkeypatch, variant):
     # H = 16384: 256 K steps in the projections, 64 column tiles in dHidden
     # and dW; V = 262144 (a 256K vocabulary): 1024 vocabulary tiles and

@@ -1,8 +1,11 @@
 """The N > 1 path of bench.py on CPU ranks (gloo, world size 2).
 
-Each rank scores its own batch with no collective on the data path; the
-only exchange is the reduction of the timing (max over ranks) and of the
-kept-row count (sum over ranks) that bench.py reports.
+Each rank scores its own batch; the data path's one exchange is the
+all-reduce of the weight gradient after the backward (the library's
+allreduce_weight_grad, run here on CPU tensors with the oracle's per-rank
+gradients), and bench.py reduces the timing (max over ranks) and the
+kept-row count (sum over ranks).  How bench.py treats --gpus is checked
+without starting ranks.
 """
 
 import os
@@ -94,3 +97,69 @@ def test_vocab_parallel_exchange_on_two_gloo_ranks():
             assert p.exitcode == 0
         for r in range(world):
             assert out[r] < 1e-12
+
+
+def _dp_rank(rank, world, port, out):
+    # data-parallel backward on CPU ranks: each rank takes its half of the
+    # batch, computes its weight gradient (the oracle stands in for the GPU
+    # backward), and allreduce_weight_grad sums them: the result must be the
+    # whole batch's weight gradient on every rank
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from oracle import lmhead_oracle as O
+    from sft_keep_mask_gb300.api import allreduce_weight_grad
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rng = np.random.default_rng(81)
+    N, H, V = 60, 16, 70
+    h = rng.standard_normal((N, H))
+    W = rng.standard_normal((V, H)) / 4.0
+    y = rng.integers(0, V, N)
+    keep = (rng.random(N) < 0.6).astype(np.uint8)
+    g_lp = rng.standard_normal(N)
+    g_ent = 0.1 * rng.standard_normal(N)
+    rows = slice(0, 27) if rank == 0 else slice(27, N)
+    _, dW_mine = O.backward(h[rows], W, y[rows], keep[rows], g_lp[rows], g_ent[rows])
+    dW = torch.from_numpy(dW_mine.copy())
+    allreduce_weight_grad(dW)
+    _, dW_all = O.backward(h, W, y, keep, g_lp, g_ent)
+    out[rank] = (float(np.abs(dW.numpy() - dW_all).max()), float(np.abs(dW_all).max()),
+                 float(np.abs(dW_mine - dW_all).max()))
+    dist.destroy_process_group()
+
+
+def test_data_parallel_weight_gradient_on_two_gloo_ranks():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        procs = [ctx.Process(target=_dp_rank, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        for r in range(world):
+            err, scale, own = out[r]
+            assert err < 1e-12 * max(scale, 1.0)
+            assert own > 1e-3 * scale  # one rank's half alone is not the answer
+
+
+def test_allreduce_weight_grad_without_a_process_group_is_the_identity():
+    import torch
+    from sft_keep_mask_gb300.api import allreduce_weight_grad
+    g = torch.arange(6.0).reshape(2, 3)
+    assert torch.equal(allreduce_weight_grad(g.clone()), g)
+
+
+def test_gpus_flag_is_honoured():
+    import bench
+    assert bench.launch_plan(1, {}) == "run"
+    assert bench.launch_plan(4, {}) == "spawn"           # no launcher: start 4 ranks
+    assert bench.launch_plan(2, {"WORLD_SIZE": "2"}) == "run"
+    assert bench.launch_plan(1, {"WORLD_SIZE": "1"}) == "run"
+    assert "8" in bench.launch_plan(8, {"WORLD_SIZE": "2"})  # never report n_gpus != N
+    assert bench.launch_plan(0, {}) != "run"
