@@ -62,8 +62,9 @@ def kernel_source_digest():
 
 
 def recorded_traffic(kernel, config):
-    """DRAM bytes per launch of `kernel` from an ncu capture of this workload,
-    or None if no capture of the current kernel sources exists."""
+    """DRAM bytes per launch of `kernel` for this workload from an ncu capture
+    (of a smaller case of it, scaled as the record states), or None if no
+    capture of the current kernel sources exists for this workload."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -75,7 +76,9 @@ def recorded_traffic(kernel, config):
     for key in ("workload", "N", "H", "V", "chunk_rows", "mode", "keep_mask", "rows", "entropy"):
         if rec.get("config", {}).get(key) != config.get(key):
             return None
-    return rec.get("kernels", {}).get(kernel)
+    k = rec.get("kernels", {}).get(kernel)
+    return None if k is None else dict(k, scaling=rec.get("scaling", ""),
+                                       capture=rec.get("capture", {}))
 
 
 def _dist():
@@ -196,17 +199,23 @@ def _oracle_sample(inp, keep, rows, want_grad=True):
 def cpu_oracle_rate(inp, keep_np, W64, rows, mode="fwdbwd", entropy_grad=True):
     """Oracle time for `rows` sampled kept rows: the forward, plus for
     mode "fwdbwd" the dhidden and dW contributions (with the entropy term
-    when `entropy_grad`)."""
-    from oracle import lmhead_oracle as O
+    when `entropy_grad`).  The timed oracle is the C float64 one (plain
+    loops, OpenMP over the host's cores)."""
+    from oracle import lmhead_oracle_c as OC
     h, y, g1, g2 = _oracle_sample(inp, keep_np, rows)
     if mode != "fwdbwd":
         g1 = g2 = None
     elif not entropy_grad:
         g2 = None
     t0 = time.perf_counter()
-    O.score_rows(h, W64, y, g1, g2)
+    OC.score_rows(h, W64, y, g1, g2)
     dt = time.perf_counter() - t0
     return rows / dt, dt
+
+
+def _oracle_cores():
+    from oracle import lmhead_oracle_c as OC
+    return OC.threads()
 
 
 L2_BYTES = 126.5e6
@@ -307,10 +316,10 @@ def run_reference(args):
         "config": dict(run_config(args, w.N, w.H, w.V, nk, world, ent_grad),
                        sample_rows_per_step=rows),
         "tflops": flops / tot / 1e12,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _oracle_cores(), "kind": "oracle",
                          "sample": f"{rows} kept rows per step, full H and V, forward"
                                    + (" + dhidden + dW contribution" if args.mode == "fwdbwd"
-                                      else "") + ", float64 numpy"},
+                                      else "") + ", C float64 oracle (OpenMP)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -494,9 +503,9 @@ def run_ours(args):
         rows = min(args.cpu_rows, nk)
         rate, dt = cpu_oracle_rate(inp, keep_np, W64, rows, args.mode, g_ent is not None)
         what = "forward + dhidden + dW contribution" if args.mode == "fwdbwd" else "forward"
-        cpu = {"value": rate, "unit": UNIT, "cores": _cores(), "kind": "oracle",
-               "sample": f"{rows} kept rows, full H and V: {what} in float64 numpy "
-                         f"({dt:.1f} s)"}
+        cpu = {"value": rate, "unit": UNIT, "cores": _oracle_cores(), "kind": "oracle",
+               "sample": f"{rows} kept rows, full H and V: {what} in the C float64 oracle "
+                         f"(OpenMP, {dt:.1f} s)"}
 
     if rank == 0:
         line = {
@@ -522,10 +531,11 @@ def run_ours(args):
         rec = recorded_traffic(roof["kernel"], line["config"])
         if rec is not None:
             roof["traffic"] = rec["dram_bytes_per_launch"]
+            cap = rec["capture"]
             roof["traffic_note"] = (
-                "ncu dram__bytes_read.sum + dram__bytes_write.sum of this kernel over one step "
-                "of this workload / its launches per step (capture of the current sources); "
-                f"algorithmic bytes per launch {rec['algorithmic_bytes_per_launch']:.4g}")
+                "ncu dram__bytes_read.sum + dram__bytes_write.sum of this kernel (current sources) "
+                f"on the same workload at V = {cap.get('V')}: {rec['scaling']}; algorithmic "
+                f"bytes per launch {rec['algorithmic_bytes_per_launch']:.4g}")
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -615,11 +625,11 @@ def main():
                     help="score the active 256-row tiles in place instead of compacting")
     ap.add_argument("--active-frac", type=float, default=1.0,
                     help="active suffix fraction of the entropy_bonus workload")
-    ap.add_argument("--ref-rows", type=int, default=256,
+    ap.add_argument("--ref-rows", type=int, default=32,
                     help="kept rows the oracle scores per step of --impl reference")
-    ap.add_argument("--cpu-rows", type=int, default=1024,
-                    help="kept rows of the cpu_baseline sample (about 12 s of oracle work "
-                         "at the default shape)")
+    ap.add_argument("--cpu-rows", type=int, default=128,
+                    help="kept rows of the cpu_baseline sample (10-30 s of oracle work "
+                         "at the default shape on 8-16 cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -51,4 +51,4 @@ def test_reference_arm_prints_the_contract_line():
     cfg = line["config"]
     want = bench.run_config(args, cfg["N"], cfg["H"], cfg["V"], cfg["kept_rows"], 1, True)
     assert {k: cfg[k] for k in want} == want
-    assert cfg["sample_rows_per_step"] == cfg["kept_rows"]  # tiny: fewer kept rows than 256
+    assert cfg["sample_rows_per_step"] == min(32, cfg["kept_rows"])  # --ref-rows default
