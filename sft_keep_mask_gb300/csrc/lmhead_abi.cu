@@ -288,11 +288,15 @@ int gemm_grid(int64_t tiles) {
 }
 
 // GEMM variant of one contraction.  By default the projections (kFwd, kDz)
-// and dW run on CTA pairs with 256 x 256 tiles and double-buffered
-// accumulators (their K = H or the chunk's rows is short, so the epilogue of
-// one tile must hide behind the MMAs of the next), and dHidden on CTA pairs
-// with 256 x 512 tiles (K = V is long: one 512-column accumulator, a third
-// fewer operand bytes per FLOP and half the passes over W).
+// run on CTA pairs with 256 x 256 tiles and double-buffered accumulators
+// (K = H is short and their epilogue (an exponential per logit) is long, so
+// it must hide behind the MMAs of the next tile), and dHidden and dW on CTA
+// pairs with 256 x 512 tiles (K = V, K = the chunk's rows: one 512-column
+// accumulator released in halves, a third fewer operand bytes per FLOP).
+// Measured on the fwd + bwd step under the power cap (same-box A/B): the
+// half-kept 64K-token step 95.3 ms against 95.6 (dHidden alone on wide
+// tiles) and 96.8 (all on 256 x 256), long context 259.5 / 264.7 / 272.4 ms;
+// the projections on wide tiles lose 7% each.
 //   LMHEAD_GEMM = "single" (one-CTA kernel, 128 x 256 tiles), "pair" or
 //     "wide" puts every contraction on one variant;
 //   LMHEAD_WIDE = a comma-separated subset of "fwd,dz,dh,dw" replaces the
@@ -319,7 +323,7 @@ GemmVariant gemm_variant(int mode) {
   if (e != nullptr && std::strcmp(e, "wide") == 0) return GemmVariant::kWide;
   static const char* kNames[4] = {"fwd", "dz", "dh", "dw"};
   const char* w = std::getenv("LMHEAD_WIDE");
-  const bool wide = w != nullptr ? listed(w, kNames[mode]) : mode == kDh;
+  const bool wide = w != nullptr ? listed(w, kNames[mode]) : (mode == kDh || mode == kDw);
   return wide ? GemmVariant::kWide : GemmVariant::kPair;
 }
 

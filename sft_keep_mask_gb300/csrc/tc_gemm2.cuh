@@ -16,8 +16,11 @@
 //             half, so a K step stages 48 KB per CTA for twice the FLOPs --
 //             a third fewer operand bytes per FLOP than NSUB = 1 -- and, with
 //             twice the output in flight, the column operand streams past
-//             half as often.  The epilogue no longer overlaps the next tile's
-//             MMAs, which pays where K is long (dHidden: K = V).  Four stages.
+//             half as often.  The accumulator is released in two 256-column
+//             halves, so the next tile's MMAs into the first half overlap the
+//             epilogue's drain of the second; the drain of the first half is
+//             not overlapped, which pays where K is long (dHidden: K = V; dW:
+//             K = the chunk's rows).  Four stages.
 //
 //   warp 0      TMA producer of this CTA's halves; both CTAs count the bytes
 //               on the even CTA's full barrier
@@ -198,35 +201,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
         const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
 
-        const int acc = it % kNumAcc;
-        const uint32_t use = static_cast<uint32_t>(it / kNumAcc);
-        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status, kSiteIssuerTmemEmpty))
-          break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kSiteIssuerFull)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a_addr = smem_addr(sA + stage * kPairABytes);
-          const uint32_t b_addr = smem_addr(sB + stage * kBStage);
+        // the MMAs of one K step into one 256-column block of the accumulator
+        auto issue = [&](int st, int kbv, int h, uint32_t d_tmem) {
+          const uint32_t a_addr = smem_addr(sA + st * kPairABytes);
+          const uint32_t bh = smem_addr(sB + st * kBStage) + static_cast<uint32_t>(h * kPairBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
                                      : smem_desc_sw128(a_addr + k * 32, 16, 1024);
-#pragma unroll
-            for (int h = 0; h < NSUB; ++h) {
-              const uint32_t bh = b_addr + static_cast<uint32_t>(h * kPairBBytes);
-              const uint64_t bd = b_mn ? smem_desc_sw128(bh + k * 2048, 8192, 1024)
-                                       : smem_desc_sw128(bh + k * 32, 16, 1024);
-              umma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN), ad, bd, idesc,
-                             (kb != kb0 || k != 0) ? 1u : 0u);
-            }
+            const uint64_t bd = b_mn ? smem_desc_sw128(bh + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(bh + k * 32, 16, 1024);
+            umma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN), ad, bd, idesc,
+                           (kbv != kb0 || k != 0) ? 1u : 0u);
           }
-          umma_commit_pair(&empty[stage], 0x3);
-          if (++stage == kStg) { stage = 0; phase ^= 1u; }
+        };
+        if (NSUB == 1) {
+          const int acc = it & 1;
+          const uint32_t use = static_cast<uint32_t>(it >> 1);
+          if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status,
+                         kSiteIssuerTmemEmpty))
+            break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kSiteIssuerFull)) { ok = false; break; }
+            tc_fence_after();
+            issue(stage, kb, 0, d_tmem);
+            umma_commit_pair(&empty[stage], 0x3);
+            if (++stage == kStg) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          umma_commit_pair(&tfull[acc], 0x3);
+        } else {
+          // One 512-column accumulator released in two 256-column halves
+          // (tempty[0], tempty[1]) as the previous tile's epilogue drains
+          // them.  The first-half MMAs of each K step start as soon as half 0
+          // is free; the second-half MMAs of the filled stages are held, in K
+          // order, until half 1 is free, and a stage is released only after
+          // both halves have read it.  When every stage is held the issuer
+          // waits for half 1, so the producer always gets a stage back.
+          const uint32_t par = (static_cast<uint32_t>(it) & 1u) ^ 1u;
+          if (!mbar_wait(&tempty[0], par, abort_flag, p.status, kSiteIssuerTmemEmpty)) break;
+          tc_fence_after();
+          bool hi = mbar_test_wait(&tempty[1], par);
+          int held = 0, hstage = 0, hkb = 0;  // held stages: count, first stage, its K block
+          auto release_held = [&]() {
+            for (int i = 0; i < held; ++i) {
+              const int st = (hstage + i) % kStg;
+              issue(st, hkb + i, 1, tmem_base);
+              umma_commit_pair(&empty[st], 0x3);
+            }
+            held = 0;
+          };
+          if (hi) tc_fence_after();
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kSiteIssuerFull)) { ok = false; break; }
+            tc_fence_after();
+            issue(stage, kb, 0, tmem_base);
+            if (!hi) {
+              hi = mbar_test_wait(&tempty[1], par);
+              if (!hi && held + 1 == kStg) {
+                if (!mbar_wait(&tempty[1], par, abort_flag, p.status, kSiteIssuerTmemEmpty)) {
+                  ok = false;
+                  break;
+                }
+                hi = true;
+              }
+              if (hi) tc_fence_after();
+            }
+            if (hi) {
+              release_held();
+              issue(stage, kb, 1, tmem_base);
+              umma_commit_pair(&empty[stage], 0x3);
+            } else {
+              if (held == 0) {
+                hstage = stage;
+                hkb = kb;
+              }
+              ++held;
+            }
+            if (++stage == kStg) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          if (held > 0) {
+            if (!mbar_wait(&tempty[1], par, abort_flag, p.status, kSiteIssuerTmemEmpty)) break;
+            tc_fence_after();
+            release_held();
+          }
+          umma_commit_pair(&tfull[0], 0x3);
         }
-        if (!ok) break;
-        umma_commit_pair(&tfull[acc], 0x3);
       }
       umma_commit_pair(drain, 0x1);
       mbar_wait_drain(drain, 0, p.status, kSiteIssuerDrain);
@@ -251,15 +314,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
-      const uint32_t te = map_to_cta(smem_addr(&tempty[acc]), 0);
-      // the tile's 256-column blocks in turn; the accumulator is released
-      // after the last TMEM load of the last block
+      // the tile's 256-column blocks in turn, each released right after its
+      // last TMEM load (one accumulator of two halves when NSUB = 2)
 #pragma unroll 1
       for (int h = 0; h < NSUB; ++h) {
-        const bool last = h == NSUB - 1;
+        const uint32_t te = map_to_cta(smem_addr(&tempty[NSUB == 1 ? acc : h]), 0);
         epilogue_tile<MODE>(p, tbase + static_cast<uint32_t>(h * kBN), mt * kPairTileM + row_local,
                             nt * NSUB + h, cstart, rows_valid, num_kb > 0, sidx, splits, os, [&] {
-                              if (!last) return;
                               tc_fence_before();
                               __syncwarp();
                               if (lane == 0) mbar_arrive_cluster(te);

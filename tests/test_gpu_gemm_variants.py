@@ -1,7 +1,7 @@
 """The GPU parity suites again with every contraction on one GEMM variant.
 
-By default dHidden runs on CTA pairs with 256 x 512 tiles and the other
-contractions on CTA pairs with 256 x 256 tiles.  LMHEAD_GEMM=single, =pair or
+By default dHidden and dW run on CTA pairs with 256 x 512 tiles and the
+projections on CTA pairs with 256 x 256 tiles.  LMHEAD_GEMM=single, =pair or
 =wide puts all four contractions on the one-CTA (128 x 256 tiles), CTA-pair
 (256 x 256) or wide CTA-pair (256 x 512) kernel; they share the epilogues and
 must give the same results.  A few parity tests pick a variant
