@@ -627,9 +627,9 @@ def main():
                     help="active suffix fraction of the entropy_bonus workload")
     ap.add_argument("--ref-rows", type=int, default=32,
                     help="kept rows the oracle scores per step of --impl reference")
-    ap.add_argument("--cpu-rows", type=int, default=128,
-                    help="kept rows of the cpu_baseline sample (10-30 s of oracle work "
-                         "at the default shape on 8-16 cores)")
+    ap.add_argument("--cpu-rows", type=int, default=256,
+                    help="kept rows of the cpu_baseline sample (about 16 s of oracle work "
+                         "at the default shape on 16 Arm cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
