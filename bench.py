@@ -342,8 +342,12 @@ def run_ours(args):
     L.lib()
 
     w = _workload(args)
-    w = synth.workload(args.workload, N=w.N, V=w.V, seed=w.seed + 100 * rank)
-    inp = synth.make_inputs(w, device=dev, active_frac=args.active_frac)
+    base_seed = w.seed
+    if world > 1:
+        # data-parallel ranks: one weight, a batch per rank
+        w = synth.workload(args.workload, N=w.N, V=w.V, seed=w.seed + 100 * rank)
+    inp = synth.make_inputs(w, device=dev, active_frac=args.active_frac,
+                            weight_seed=base_seed if world > 1 else None)
     sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=args.chunk_rows, device=dev,
                       blocksparse=args.blocksparse)
     comps = inp.get("components")

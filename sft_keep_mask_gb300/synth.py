@@ -112,8 +112,12 @@ def _spans(rng: np.random.Generator, w: Workload, active_frac: float):
 
 
 def make_inputs(w: Workload, device="cpu", active_frac: float = 1.0,
-                keep_all: bool = False):
+                keep_all: bool = False, weight_seed=None):
     """Draw one batch of the workload.
+
+    weight_seed: draw W from its own generator with this seed (data-parallel
+    ranks share the weight and draw their batches from per-rank seeds);
+    None draws it from the workload's generator, between hidden and targets.
 
     Returns a dict with
       hidden [N,H] bf16, weight [V,H] bf16, targets [N] int64,
@@ -131,9 +135,13 @@ def make_inputs(w: Workload, device="cpu", active_frac: float = 1.0,
     hidden = hidden.to(torch.bfloat16)
     std = w.w_scale / float(np.sqrt(w.H))
     weight = torch.empty(w.V, w.H, device=dev, dtype=torch.bfloat16)
+    gw = g
+    if weight_seed is not None:
+        gw = torch.Generator(device=dev)
+        gw.manual_seed(weight_seed)
     rows = 8192
     for r in range(0, w.V, rows):
-        blk = torch.randn(min(rows, w.V - r), w.H, generator=g, device=dev,
+        blk = torch.randn(min(rows, w.V - r), w.H, generator=gw, device=dev,
                           dtype=torch.float32)
         weight[r:r + blk.shape[0]] = (blk * std).to(torch.bfloat16)
     targets = torch.randint(0, w.V, (w.N,), generator=g, device=dev, dtype=torch.int64)

@@ -163,3 +163,22 @@ def test_gpus_flag_is_honoured():
     assert bench.launch_plan(1, {"WORLD_SIZE": "1"}) == "run"
     assert "8" in bench.launch_plan(8, {"WORLD_SIZE": "2"})  # never report n_gpus != N
     assert bench.launch_plan(0, {}) != "run"
+
+
+def test_data_parallel_ranks_share_the_weight_and_not_the_batch():
+    # bench.py's ranks draw their batches from per-rank seeds and the weight
+    # from the workload's seed, as data-parallel replicas of one model
+    from sft_keep_mask_gb300 import synth
+    base = synth.workload("tiny", N=64, H=16, V=50)
+    r0 = synth.make_inputs(synth.workload("tiny", N=64, H=16, V=50, seed=base.seed), "cpu",
+                           weight_seed=base.seed)
+    r1 = synth.make_inputs(synth.workload("tiny", N=64, H=16, V=50, seed=base.seed + 100),
+                           "cpu", weight_seed=base.seed)
+    import torch
+    assert torch.equal(r0["weight"], r1["weight"])
+    assert not torch.equal(r0["hidden"], r1["hidden"])
+    # and each draw is reproducible
+    again = synth.make_inputs(synth.workload("tiny", N=64, H=16, V=50, seed=base.seed + 100),
+                              "cpu", weight_seed=base.seed)
+    assert torch.equal(r1["hidden"], again["hidden"]) and torch.equal(r1["weight"],
+                                                                      again["weight"])
