@@ -58,7 +58,8 @@
  *     "wide" runs all four contractions on the one-CTA (128 x 256 tiles),
  *     CTA-pair (256 x 256 tiles, two accumulators) or wide CTA-pair (256 x
  *     512 tiles, one accumulator) tcgen05 kernel; unset, dHidden and dW run on
- *     wide tiles and the projections on 256 x 256 tiles, unless LMHEAD_WIDE names
+ *     wide tiles when H spans an even number of 256-column tiles, and
+ *     everything else on 256 x 256 tiles, unless LMHEAD_WIDE names
  *     the contractions on wide tiles ("fwd,dz,dh,dw" or a subset, "none").
  *     LMHEAD_DH_SPLIT = 1 .. 4 caps the K split of dHidden (default 4).  The
  *     variants accumulate in the same order and differ at most by the K split

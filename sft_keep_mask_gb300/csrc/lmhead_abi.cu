@@ -292,7 +292,8 @@ int gemm_grid(int64_t tiles) {
 // (K = H is short and their epilogue (an exponential per logit) is long, so
 // it must hide behind the MMAs of the next tile), and dHidden and dW on CTA
 // pairs with 256 x 512 tiles (K = V, K = the chunk's rows: one 512-column
-// accumulator released in halves, a third fewer operand bytes per FLOP).
+// accumulator released in halves, a third fewer operand bytes per FLOP) when
+// H spans an even number of 256-column tiles (H = 2560, 4096, 5120, ...).
 // Measured on the fwd + bwd step under the power cap (same-box A/B): the
 // half-kept 64K-token step 95.3 ms against 95.6 (dHidden alone on wide
 // tiles) and 96.8 (all on 256 x 256), long context 259.5 / 264.7 / 272.4 ms;
@@ -316,15 +317,18 @@ bool listed(const char* list, const char* name) {
   return false;
 }
 
-GemmVariant gemm_variant(int mode) {
+GemmVariant gemm_variant(int mode, int H) {
   const char* e = std::getenv("LMHEAD_GEMM");
   if (e != nullptr && std::strcmp(e, "single") == 0) return GemmVariant::kSingle;
   if (e != nullptr && std::strcmp(e, "pair") == 0) return GemmVariant::kPair;
   if (e != nullptr && std::strcmp(e, "wide") == 0) return GemmVariant::kWide;
   static const char* kNames[4] = {"fwd", "dz", "dh", "dw"};
   const char* w = std::getenv("LMHEAD_WIDE");
-  const bool wide = w != nullptr ? listed(w, kNames[mode]) : (mode == kDh || mode == kDw);
-  return wide ? GemmVariant::kWide : GemmVariant::kPair;
+  if (w != nullptr) return listed(w, kNames[mode]) ? GemmVariant::kWide : GemmVariant::kPair;
+  // dHidden and dW tile the H columns: with an odd number of 256-column tiles
+  // the last 512-column tile would spend half its MMAs on columns past H
+  const bool h_even = cdiv(H, kBN) % 2 == 0;
+  return (mode == kDh || mode == kDw) && h_even ? GemmVariant::kWide : GemmVariant::kPair;
 }
 
 // Rows and columns of one tile of the selected variant.
@@ -418,7 +422,7 @@ lmhead_status fwd_impl(const void* hidden, const void* weight, const int64_t* ta
   }
   if (st != LMHEAD_OK) return st;
 
-  const GemmVariant gv = gemm_variant(kFwd);
+  const GemmVariant gv = gemm_variant(kFwd, H);
   CUtensorMap ma, mb, mb2;
   if (!(blocksparse ? make_map(&ma, hidden, N, H, H, kBM, 64)
                     : make_map(&ma, hc, L.C, H, H, kBM, 64)) ||
@@ -542,9 +546,9 @@ lmhead_status bwd_impl(const void* hidden, const void* weight, const int64_t* ta
     LM_TRY(launch_zero_skipped_rows(keep, N, H, static_cast<__nv_bfloat16*>(dhidden), s));
   }
 
-  const GemmVariant gv_dz = gemm_variant(kDz);
-  const GemmVariant gv_dh = gemm_variant(kDh);
-  const GemmVariant gv_dw = gemm_variant(kDw);
+  const GemmVariant gv_dz = gemm_variant(kDz, H);
+  const GemmVariant gv_dh = gemm_variant(kDh, H);
+  const GemmVariant gv_dw = gemm_variant(kDw, H);
   CUtensorMap m_hc_k, m_w_k, m_w_k2, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn, m_dz_out, m_dw_out;
   const void* rows_src = blocksparse ? hidden : static_cast<const void*>(hc);
   const int64_t rows_n = blocksparse ? N : L.C;
