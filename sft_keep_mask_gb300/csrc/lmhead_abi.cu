@@ -292,7 +292,7 @@ int gemm_grid(int64_t tiles) {
 // (K = H is short and their epilogue (an exponential per logit) is long, so
 // it must hide behind the MMAs of the next tile), and dHidden and dW on CTA
 // pairs with 256 x 512 tiles (K = V, K = the chunk's rows: one 512-column
-// accumulator released in halves, a third fewer operand bytes per FLOP) when
+// accumulator released in halves, a quarter fewer operand bytes per FLOP) when
 // H spans an even number of 256-column tiles (H = 2560, 4096, 5120, ...).
 // Measured on the fwd + bwd step under the power cap (same-box A/B): the
 // half-kept 64K-token step 95.3 ms against 95.6 (dHidden alone on wide

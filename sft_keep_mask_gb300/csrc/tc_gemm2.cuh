@@ -14,7 +14,7 @@
 //   NSUB = 2  256 x 512 tiles in one 512-column accumulator (all of TMEM):
 //             each 64-wide K step issues two N = 256 MMAs that share the A
 //             half, so a K step stages 48 KB per CTA for twice the FLOPs --
-//             a third fewer operand bytes per FLOP than NSUB = 1 -- and, with
+//             a quarter fewer operand bytes per FLOP than NSUB = 1 -- and, with
 //             twice the output in flight, the column operand streams past
 //             half as often.  The accumulator is released in two 256-column
 //             halves, so the next tile's MMAs into the first half overlap the
