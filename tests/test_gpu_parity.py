@@ -234,6 +234,46 @@ def test_full_size_qwen3_4b_forward_sampled():
     _sampled_rows_check(w, inp, keep, dict(lp=lp, ent=ent, lse=lse), 48, False)
 
 
+def test_row_offsets_past_two_to_the_31_elements():
+    # N x H = 2.46e9 elements: every kept row from 2^31 / H = 524288 on starts
+    # past the 32-bit element range of hidden and dhidden.  Only kept rows are
+    # read, so the others stay zero; V is small so that the oracle checks the
+    # whole dW and every kept row.
+    N, H, V = 600000, 4096, 3000
+    first_far = (1 << 31) // H
+    rng = np.random.default_rng(2031)
+    near = rng.choice(first_far, 1000, replace=False)
+    far = first_far + rng.choice(N - first_far, 1000, replace=False)
+    kept = np.sort(np.concatenate([near, far]))
+    keep_np = np.zeros(N, np.uint8)
+    keep_np[kept] = 1
+    g = torch.Generator(device=DEV).manual_seed(2031)
+    hidden = torch.zeros(N, H, dtype=torch.bfloat16, device=DEV)
+    rows = torch.from_numpy(kept).to(DEV)
+    hidden[rows] = torch.randn(len(kept), H, generator=g, device=DEV).to(torch.bfloat16)
+    weight = (torch.randn(V, H, generator=g, device=DEV) / math.sqrt(H)).to(torch.bfloat16)
+    targets = torch.randint(0, V, (N,), generator=g, device=DEV)
+    g_lp = torch.randn(N, generator=g, device=DEV)
+    g_ent = 0.1 * torch.randn(N, generator=g, device=DEV)
+    keep = torch.from_numpy(keep_np).to(DEV)
+    sc = LMHeadScorer(N, H, V)
+    lp, ent, lse = sc.forward(hidden, weight, targets, keep)
+    dh, dW = sc.backward(hidden, weight, targets, keep, lse, ent, g_lp, g_ent)
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    olp, oent, olse, odh, odW = O.score_rows(to64(hidden[rows]), to64(weight),
+                                             targets[rows].cpu().numpy(),
+                                             g_lp[rows].cpu().double().numpy(),
+                                             g_ent[rows].cpu().double().numpy())
+    assert_rows_close(lp[rows].cpu().double().numpy(), olp, "logprob (rows past 2^31 elements)")
+    assert_rows_close(ent[rows].cpu().double().numpy(), oent, "entropy")
+    assert_rows_close(lse[rows].cpu().double().numpy(), olse, "lse")
+    assert_frob_close(to64(dh[rows]), odh, "dhidden (rows past 2^31 elements)")
+    assert_frob_close(dW.cpu().double().numpy(), odW, "dW")
+    skipped = torch.from_numpy(np.flatnonzero(keep_np == 0)[-1000:]).to(DEV)  # far rows
+    assert (dh[skipped] == 0).all() and (lp[skipped] == 0).all()
+
+
 def test_full_size_qwen3_4b_forward_backward_metric_only_sampled():
     # the Qwen3-4B head's fwd + bwd with the entropy as a metric only (no
     # entropy gradient, [P2] How it works): sampled rows against the oracle
