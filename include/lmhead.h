@@ -211,9 +211,10 @@ lmhead_status lmhead_bwd(const void* hidden, const void* weight, const int64_t* 
  * The first call on a device looks up the array's device address (a one-time
  * set-up per device and CUDA context, done with that device current; a new
  * context on the device, e.g. after cudaDeviceReset, gets a fresh look-up);
- * make that first call before any stream capture.  Every call on a device shares the one array and
- * it keeps the last call's contents: calls whose work overlaps on the GPU
- * (e.g. on two streams at once) race and must be ordered by the caller.
+ * make that first call before any stream capture.  Every call on a device
+ * shares the one array and it keeps the last call's contents: calls whose
+ * work overlaps on the GPU (e.g. on two streams at once) race and must be
+ * ordered by the caller.
  */
 lmhead_status lmhead_compact_noalloc(const uint8_t* keep, const int64_t* targets, int64_t N,
                                      int V, int32_t* idx, int32_t* targets_c, int32_t* d_nk,
