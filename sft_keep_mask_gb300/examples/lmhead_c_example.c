@@ -87,7 +87,17 @@ int main(void) {
   CHECK_LM(lmhead_fwd(dh, dw, dy, dkeep, N, H, V, 1, dlp, dent, dlse, 0, ws, wsb, NULL));
   CHECK_LM(lmhead_bwd(dh, dw, dy, dkeep, N, H, V, dlse, dent, dg, NULL, ddh, ddw, 0, 0, ws, wsb,
                       NULL));
-  CHECK_LM(lmhead_get_status(ws, NULL));
+  {
+    /* a device-side error (a bad target, a pipeline wait that ran out) is
+       reported here; on a timeout the record names the wait that gave up */
+    const lmhead_status st = lmhead_get_status(ws, NULL);
+    if (st != LMHEAD_OK) {
+      const int32_t rec = lmhead_get_timeout_record(ws, NULL);
+      fprintf(stderr, "device status: %s (timeout record: site %d, cta %d)\n",
+              lmhead_strerror(st), rec > 0 ? rec >> 24 : 0, rec > 0 ? rec & 0xFFFFFF : 0);
+      return 3;
+    }
+  }
 
   float* lp = malloc(N * 4);
   float* ent = malloc(N * 4);
