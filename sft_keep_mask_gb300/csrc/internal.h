@@ -94,8 +94,9 @@ struct TcGemmParams {
   float4* part;             // kFwd: [ceil(V/kBN)][C] (m, s, u, t)
   __nv_bfloat16* dhidden;   // kDh: [N, H]
   int beta;                 // kDw: 1 = add to dW (the output map's tensor)
-  float* dh_part;           // kDh split over K: [max_split][C][H] fp32 partial sums
-  int max_split;            // kDh: largest K split (1 = never split)
+  float* dh_part;           // kDh: [max_split][C][H] fp32 partial sums of split
+                            //   tiles, by part (work_schedule)
+  int max_split;            // kDh: most K parts of a tile (1 = never split K)
   int split_fill_pct;       // kDh: split only below this fill of the worker slots
   int stall;                // fault injection: the producer issues no loads, so
                             //   the pipeline waits run out (device ETIMEOUT)
@@ -146,31 +147,106 @@ __host__ __device__ __forceinline__ void chunk_span(int nk, int C, int c, int& s
   rows = nk - start < cb ? nk - start : cb;
 }
 
-// Number of K splits of the dHidden contraction (K = V is long, the tile grid
-// is small).  Unsplit, the last wave of `workers` persistent CTAs (or CTA
-// pairs) is partly idle; measured on GB300, that tail costs less than its
-// share of tiles (the few workers left run faster), so the contraction is split
-// only when fewer than 85% of the worker-slots hold a tile -- then into the
-// S <= max_split that fills the slots best (the smallest S among equals).
-// With S > 1 the contraction writes fp32 partials that a reduction adds up.
-__host__ __device__ __forceinline__ int dh_split_count(int tiles, int workers, int num_kb,
-                                                      int max_split, int min_fill_pct = 85) {
-  if (tiles <= 0 || workers <= 0) return 1;
+// Work schedule of one persistent GEMM launch over `tiles` output tiles of
+// `num_kb` K blocks each, taken by `workers` persistent workers (CTA pairs or
+// CTAs) in units of one tile and a range of its K blocks.  Worker w takes
+// units w, w + W, w + 2W, ..., so the units in flight at any time are
+// neighbours in unit order and walk their K ranges in step: the operand
+// slices they share are read from DRAM once and then from L2.
+//
+// Plain: every unit is one whole tile.  Every contraction but dHidden, and
+// dHidden when the last wave of tiles fills at least fill_pct of the worker
+// slots (measured on GB300, a partly idle last wave costs less than its share
+// of tiles: the few workers left run faster).
+//
+// Split tail (dHidden otherwise; K = V is long and the tile grid small): the
+// tiles of the whole waves stay whole, and each of the R tiles of the last
+// wave is cut into S equal K parts, so the last wave takes 1/S of a whole
+// tile's time (S in 2 .. max_split, chosen for the fewest tail rounds per
+// part; R * S units may take more than one round).  Parts with the same index
+// share their K range, so the tail walks K in step too.  Its tiles get S fp32
+// partial sums, slot p for part p, that the dHidden reduction adds in slot
+// order; whole tiles write their bf16 rows to dhidden directly.  (Cutting the
+// iterations into equal ranges per worker instead -- stream-K -- balances the
+// waves exactly, but each worker then starts at its own K offset: measured on
+// the half-kept 64K-token step, dHidden fetched so much more from DRAM that
+// the step took 3.5% longer.)
+struct WorkSched {
+  int tiles = 0;
+  int num_kb = 0;
+  int workers = 0;
+  int full = 0;        // tiles taken whole: 0 .. full-1 (all tiles when split == 1)
+  int split = 1;       // K parts of each tail tile full .. tiles-1
+
+  __host__ __device__ __forceinline__ int units() const {
+    return full + (tiles - full) * split;
+  }
+  // Units (workers' partial sums) of tile t: 1 for a tile taken whole.
+  __host__ __device__ __forceinline__ int tile_slots(int t) const {
+    return t < full ? 1 : split;
+  }
+};
+
+__host__ __device__ __forceinline__ WorkSched work_schedule(int tiles, int workers, int num_kb,
+                                                            bool may_split, int max_split,
+                                                            int fill_pct) {
+  WorkSched s;
+  s.tiles = tiles;
+  s.num_kb = num_kb;
+  s.workers = workers;
+  s.full = tiles;
+  if (!may_split || tiles <= 0 || workers <= 0 || max_split < 2 || num_kb < 2) return s;
+  const long long slots = static_cast<long long>((tiles + workers - 1) / workers) * workers;
+  if (static_cast<long long>(tiles) * 100 >= slots * fill_pct) return s;
+  const int rem = tiles % workers;  // > 0: the last wave is not full
+  // tail time in units of a whole tile's time: ceil(rem * S / W) rounds of 1/S
   int best = 1;
-  long long best_num = tiles, best_den = (long long)((tiles + workers - 1) / workers) * workers;
-  if (best_num * 100 >= best_den * min_fill_pct) return 1;
-  for (int s = 2; s <= max_split && s <= num_kb; ++s) {
-    const long long units = (long long)tiles * s;
-    const long long den = (units + workers - 1) / workers * workers;
-    // strictly better by at least 1% of a wave's worth of efficiency
-    if (units * best_den > best_num * den + den * best_den / 100) {
-      best = s;
-      best_num = units;
-      best_den = den;
+  long long best_rounds = 1;  // rounds of the unsplit tail
+  for (int S = 2; S <= max_split && S <= num_kb; ++S) {
+    const long long rounds = (static_cast<long long>(rem) * S + workers - 1) / workers;
+    if (rounds * best < best_rounds * S) {  // rounds / S < best_rounds / best
+      best = S;
+      best_rounds = rounds;
     }
   }
-  return best;
+  if (best == 1) return s;
+  s.full = tiles - rem;
+  s.split = best;
+  return s;
 }
+
+// One unit of a worker's work: K blocks [kb0, kb1) of tile `tile`, part
+// `slot` of the `slots` parts the tile is cut into.
+struct WorkSeg {
+  int tile, kb0, kb1, slot, slots;
+};
+
+// Walks one worker's units in order.  The producer, the MMA issuer and the
+// epilogue of a worker each walk them with their own iterator, so all three
+// see the same sequence.
+struct SegIter {
+  WorkSched s;
+  int u;
+
+  __host__ __device__ __forceinline__ SegIter(const WorkSched& sched, int w) : s(sched), u(w) {}
+  // Fills g with the next unit; false when the worker has no more work.
+  __host__ __device__ __forceinline__ bool next(WorkSeg& g) {
+    if (u >= s.units()) return false;
+    if (u < s.full) {
+      g = WorkSeg{u, 0, s.num_kb, 0, 1};
+    } else {
+      const int rem = s.tiles - s.full;
+      const int part = (u - s.full) / rem;
+      g.tile = s.full + (u - s.full - part * rem);
+      g.kb0 = static_cast<int>(static_cast<int64_t>(part) * s.num_kb / s.split);
+      g.kb1 = static_cast<int>(static_cast<int64_t>(part + 1) * s.num_kb / s.split);
+      g.slot = part;
+      g.slots = s.split;
+    }
+    u += s.workers;
+    return true;
+  }
+};
 
 // Block-sparse mode: row of the hidden states behind compact row (cstart + lrow),
 // where the compact rows are the rows of the active 256-row tiles in order.
@@ -222,8 +298,9 @@ cudaError_t launch_gather_vec(const int32_t* idx, const int32_t* d_nk, int64_t N
                               const float* a, const float* b, const float* c, const float* d,
                               float* a_c, float* b_c, float* c_c, float* d_c, int* status,
                               cudaStream_t s);
-// Sum of the dHidden K-split partials of one chunk, rows scattered to
-// dhidden[idx] as bf16; does nothing when the contraction was not split.
+// Sum of the dHidden partials of the chunk's split tail tiles
+// (work_schedule), rows scattered to dhidden[idx] as bf16; tiles taken whole
+// were written by the contraction itself.
 cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_index,
                              int chunk_rows, int H, int tile_m, int tile_n, int workers, int num_kb,
                              int max_split, int fill_pct, const int32_t* idx,

@@ -19,7 +19,7 @@
 namespace lmhead {
 namespace {
 
-constexpr int kDhMaxSplit = 4;  // largest K split of the dHidden contraction
+constexpr int kDhMaxSplit = 4;  // most K parts of a dHidden tile (partial buffers)
 static_assert(kDhMaxSplit <= 4, "the dHidden reduction sums at most four partials");
 constexpr int kDhSplitFillPct = 85;  // split only when fewer worker slots than this are busy
 // Raster blocks of the vocabulary projections (kFwd, kDz): 32 MB of bf16 Hc
@@ -335,8 +335,8 @@ GemmVariant gemm_variant(int mode, int H) {
 inline int tile_rows(GemmVariant v) { return v == GemmVariant::kSingle ? kBM : 256; }
 inline int tile_cols(GemmVariant v) { return v == GemmVariant::kWide ? 2 * kBN : kBN; }
 
-// Largest K split of dHidden: LMHEAD_DH_SPLIT = 1 .. 4 (default 4; 1 never
-// splits).
+// Most K parts of a dHidden tail tile (work_schedule): LMHEAD_DH_SPLIT =
+// 1 .. 4 (default 4; 1 never splits).
 int dh_max_split() {
   const char* e = std::getenv("LMHEAD_DH_SPLIT");
   if (e == nullptr) return kDhMaxSplit;
@@ -349,15 +349,15 @@ int dh_max_split() {
 // maps for the one-CTA and CTA-pair variants (they differ only for K-major
 // B); c is the output map of kDz / kDw (the other contractions do not read
 // it).  *workers receives the number of persistent workers launched (CTA
-// pairs or CTAs), which the dHidden split rule depends on.
+// pairs or CTAs), which the dHidden schedule depends on.
 template <int MODE>
 cudaError_t run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b_single,
                      const CUtensorMap& b_pair, const CUtensorMap& c, const TcGemmParams& p,
                      int64_t m_upper, int64_t n, cudaStream_t s, int* workers = nullptr) {
   if (fault_at("launch")) return cudaErrorLaunchFailure;
-  const int split = MODE == kDh ? p.max_split : 1;
+  const int share = MODE == kDh ? p.max_split : 1;  // K parts a dHidden tile may be cut into
   if (v == GemmVariant::kPair || v == GemmVariant::kWide) {
-    const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, tile_cols(v)) * split;
+    const int64_t tiles = cdiv(m_upper, 256) * cdiv(n, tile_cols(v)) * share;
     const int64_t pairs = device_info().sms / 2;
     const int64_t w = tiles < pairs ? (tiles < 1 ? 1 : tiles) : pairs;
     if (workers != nullptr) *workers = static_cast<int>(w);
@@ -365,7 +365,7 @@ cudaError_t run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b_s
                ? launch_tc_gemm_pair<MODE, 2>(a, b_pair, c, p, static_cast<int>(2 * w), s)
                : launch_tc_gemm_pair<MODE, 1>(a, b_pair, c, p, static_cast<int>(2 * w), s);
   }
-  const int grid = gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN) * split);
+  const int grid = gemm_grid(cdiv(m_upper, kBM) * cdiv(n, kBN) * share);
   if (workers != nullptr) *workers = grid;
   return launch_tc_gemm<MODE>(a, b_single, c, p, grid, s);
 }

@@ -377,38 +377,51 @@ __global__ void scatter_vals_kernel(const float* __restrict__ src, const int32_t
   dst[r] = src[k];
 }
 
+// One block per (tile, 32-row slice) of the chunk's dHidden tile grid.  Only
+// the tiles of the split tail (work_schedule) hold partial sums; the blocks
+// of the tiles taken whole return at once.  The partials are added in slot
+// (K) order, so the sum is the same on every run.
 __global__ void dh_reduce_kernel(const float4* __restrict__ part, const int32_t* d_nk,
                                  int chunk_index, int chunk_rows, int H, int tile_m, int tile_n,
-                                 int workers,
-                                 int num_kb, int max_split, int fill_pct,
+                                 int workers, int num_kb, int max_split, int fill_pct,
                                  const int32_t* __restrict__ idx,
                                  const uint8_t* __restrict__ lvalid, uint2* __restrict__ dhidden,
                                  int64_t N, int* status) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
   if (rows == 0) return;
-  const int tiles = ((rows + tile_m - 1) / tile_m) * ((H + tile_n - 1) / tile_n);
-  const int splits = dh_split_count(tiles, workers, num_kb, max_split, fill_pct);
-  if (splits == 1) return;
+  const int num_m = (rows + tile_m - 1) / tile_m;
+  const int num_n = (H + tile_n - 1) / tile_n;
+  const int t = static_cast<int>(blockIdx.x);
+  if (t >= num_m * num_n) return;
+  const WorkSched sched = work_schedule(num_m * num_n, workers, num_kb, true, max_split, fill_pct);
+  const int slots = sched.tile_slots(t);
+  if (slots < 2) return;
+  // dHidden walks its tiles row-major (tile_coords with group_m = 0 and all
+  // column tiles in one group)
+  const int mt = t / num_n;
+  const int nt = t - mt * num_n;
   const int q = H / 4;  // float4 columns per row
+  const int c0 = nt * (tile_n / 4);
+  const int cn = q - c0 < tile_n / 4 ? q - c0 : tile_n / 4;
+  const int r0 = mt * tile_m + static_cast<int>(blockIdx.y) * 32;
   const int64_t plane = static_cast<int64_t>(chunk_rows) * q;
-  const int64_t total = static_cast<int64_t>(rows) * q;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
-       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(g / q);
-    const int c = static_cast<int>(g - static_cast<int64_t>(r) * q);
+  for (int e = threadIdx.x; e < 32 * cn; e += blockDim.x) {
+    const int r = r0 + e / cn;
+    const int c = c0 + e % cn;
+    if (r >= rows) continue;
     if (lvalid != nullptr && lvalid[chunk_start + r] == 0) continue;  // not a kept row
     const int64_t at = static_cast<int64_t>(r) * q + c;
     // all partial loads in flight before the (fixed-order) sum
     float4 v[4];
 #pragma unroll
-    for (int sidx = 0; sidx < 4; ++sidx)
-      v[sidx] = sidx < splits ? __ldcs(part + sidx * plane + at) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < 4; ++k)
+      v[k] = k < slots ? __ldcs(part + k * plane + at) : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = v[0];
 #pragma unroll
-    for (int sidx = 1; sidx < 4; ++sidx) {
-      if (sidx < splits) {
-        acc.x += v[sidx].x; acc.y += v[sidx].y; acc.z += v[sidx].z; acc.w += v[sidx].w;
+    for (int k = 1; k < 4; ++k) {
+      if (k < slots) {
+        acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
       }
     }
     const int64_t orow = idx[chunk_start + r];
@@ -533,14 +546,15 @@ cudaError_t launch_dh_reduce(const float* part, const int32_t* d_nk, int chunk_i
                              int max_split, int fill_pct, const int32_t* idx,
                              const uint8_t* lvalid, __nv_bfloat16* dhidden, int64_t N,
                              int* status, cudaStream_t s) {
-  // a grid-stride loop over a grid of 4 blocks per SM: cheap when the
-  // contraction was not split and the kernel returns at once
-  const int64_t threads = static_cast<int64_t>(chunk_rows) * (H / 4);
-  const unsigned want = blocks_for(threads, 256);
-  const unsigned cap = static_cast<unsigned>(4 * (device_sm_count() > 0 ? device_sm_count() : 148));
-  dh_reduce_kernel<<<want < cap ? want : cap, 256, 0, s>>>(
-      reinterpret_cast<const float4*>(part), d_nk, chunk_index, chunk_rows, H, tile_m, tile_n, workers,
-      num_kb, max_split, fill_pct, idx, lvalid, reinterpret_cast<uint2*>(dhidden), N, status);
+  // the chunk's largest tile grid (its rows are known only on the device);
+  // blocks past the chunk's tiles, and of tiles taken whole, return
+  const int64_t tiles = static_cast<int64_t>((chunk_rows + tile_m - 1) / tile_m) *
+                        ((H + tile_n - 1) / tile_n);
+  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(tile_m / 32));
+  dh_reduce_kernel<<<grid, 256, 0, s>>>(
+      reinterpret_cast<const float4*>(part), d_nk, chunk_index, chunk_rows, H, tile_m, tile_n,
+      workers, num_kb, max_split, fill_pct, idx, lvalid, reinterpret_cast<uint2*>(dhidden), N,
+      status);
   return cudaGetLastError();
 }
 

@@ -14,7 +14,7 @@
 //         recomputed rather than saved, twinkle pull request #283, section 1),
 //         rounded to bf16 and written by TMA stores from shared memory.
 //   kDh   bf16 rows scattered to dhidden[idx[row]] (fp32 partial rows when
-//         the K range is split).
+//         the tile's K range is split into parts, see work_schedule).
 //   kDw   fp32 dW tile, written by TMA stores (first chunk) or added to dW by
 //         TMA reduce-adds at L2.
 #pragma once
@@ -121,13 +121,15 @@ __device__ __forceinline__ void out_issue(OutStage& os, uint8_t* b, int lane, in
 //   cstart     first compact row of the chunk
 //   rows_valid rows of the chunk that hold kept tokens
 //   have_acc   false only for kDw with an empty K range (writes zeros)
-//   split_idx, splits  kDh with its K range split: write fp32 partial sums
+//   slot, slots  kDh: part `slot` of the `slots` K parts of the tile
+//              (work_schedule); with slots > 1 write fp32 partial sums to
+//              partial buffer `slot`
 //   release    called once, right after the last TMEM load of the tile
 //   os         the warp's output staging (kDz, kDw)
 template <int MODE, typename Release>
 __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tbase, int row,
                                               int nt, int cstart, int rows_valid, bool have_acc,
-                                              int split_idx, int splits, OutStage& os,
+                                              int slot, int slots, OutStage& os,
                                               Release&& release) {
   constexpr int kSlices = kBN / 32;
   const int col_tile = nt * kBN;
@@ -268,7 +270,7 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
     const bool row_ok = kept && LM_DCHECK(orow >= 0 && orow < p.n_rows, p.status);
     __nv_bfloat16* hrow = p.dhidden + orow * p.H;
     float* prow = p.dh_part +
-                  (static_cast<int64_t>(split_idx) * p.chunk_rows + (row_ok ? row : 0)) * p.H;
+                  (static_cast<int64_t>(slot) * p.chunk_rows + (row_ok ? row : 0)) * p.H;
 #pragma unroll 1
     for (int c = 0; c < kSlices; ++c) {
       uint32_t r[32];
@@ -278,7 +280,7 @@ __device__ __forceinline__ void epilogue_tile(const TcGemmParams& p, uint32_t tb
       if (c == kSlices - 1) release();
       const int col = col_tile + c * 32;
       if (!row_ok || col >= p.H) continue;
-      if (splits > 1) {
+      if (slots > 1) {
         float4* dst = reinterpret_cast<float4*>(prow + col);
 #pragma unroll
         for (int v = 0; v < 8; ++v)

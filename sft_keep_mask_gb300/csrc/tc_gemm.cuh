@@ -64,9 +64,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_n = (N + kBN - 1) / kBN;
   const int num_kb = (K + kBK - 1) / kBK;
   const int num_tiles = num_m * num_n;
-  const int splits = MODE == kDh ? dh_split_count(num_tiles, static_cast<int>(gridDim.x), num_kb, p.max_split, p.split_fill_pct) : 1;
-  const int num_units = num_tiles * splits;
-  if (static_cast<int>(blockIdx.x) >= num_units) return;
+  const int worker = static_cast<int>(blockIdx.x);
+  const WorkSched sched = work_schedule(num_tiles, static_cast<int>(gridDim.x), num_kb,
+                                        MODE == kDh, p.max_split, p.split_fill_pct);
+  WorkSeg seg;
+  if (!SegIter(sched, worker).next(seg)) return;  // no work for this CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -101,15 +103,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      for (int u = blockIdx.x; u < num_units && !p.stall; u += gridDim.x) {
-        const int t = u % num_tiles;
-        const int sidx = u / num_tiles;
-        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
-        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
+      SegIter segs(sched, worker);
+      for (WorkSeg g; !p.stall && segs.next(g);) {
         int mt, nt;
-        tile_coords(t, num_m, num_n, p.group_m, p.group_n, mt, nt);
+        tile_coords(g.tile, num_m, num_n, p.group_m, p.group_n, mt, nt);
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kSiteProducerEmpty)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
           uint8_t* a_dst = sA + stage * kABytes;
@@ -156,11 +155,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok && num_kb > 0; u += gridDim.x, ++it) {
-        const int t = u % num_tiles;
-        const int sidx = u / num_tiles;
-        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
-        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
+      SegIter segs(sched, worker);
+      for (WorkSeg g; ok && num_kb > 0 && segs.next(g); ++it) {
+        const int kb0 = g.kb0;
+        const int kb1 = g.kb1;
 
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -199,11 +197,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     OutStage os{&tma_c, sOut + (warp - 2) * 2 * kOutBoxBytes, 0u};
     int it = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
-      const int t = u % num_tiles;
-      const int sidx = u / num_tiles;
+    SegIter segs(sched, worker);
+    for (WorkSeg g; segs.next(g); ++it) {
       int mt, nt;
-      tile_coords(t, num_m, num_n, p.group_m, p.group_n, mt, nt);
+      tile_coords(g.tile, num_m, num_n, p.group_m, p.group_n, mt, nt);
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       if (num_kb > 0) {
@@ -212,7 +209,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(acc * kBN);
       uint64_t* te = &tempty[acc];
-      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, cstart, rows_valid, num_kb > 0, sidx, splits, os, [&] {
+      epilogue_tile<MODE>(p, tbase, mt * kBM + row_local, nt, cstart, rows_valid, num_kb > 0, g.slot, g.slots, os, [&] {
         tc_fence_before();
         mbar_arrive(te);
       });

@@ -92,9 +92,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int num_n = (N + kTileN - 1) / kTileN;
   const int num_kb = (K + kBK - 1) / kBK;
   const int num_tiles = num_m * num_n;
-  const int splits = MODE == kDh ? dh_split_count(num_tiles, num_pairs, num_kb, p.max_split, p.split_fill_pct) : 1;
-  const int num_units = num_tiles * splits;
-  if (pair >= num_units) return;  // both CTAs of the pair leave together
+  const WorkSched sched =
+      work_schedule(num_tiles, num_pairs, num_kb, MODE == kDh, p.max_split, p.split_fill_pct);
+  WorkSeg seg;
+  if (!SegIter(sched, pair).next(seg)) return;  // no work: both CTAs of the pair leave together
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStg; ++s) {
@@ -130,15 +131,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       const int half = static_cast<int>(rank) * 128;
-      for (int u = pair; u < num_units && !p.stall; u += num_pairs) {
-        const int t = u % num_tiles;
-        const int sidx = u / num_tiles;
-        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
-        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
+      SegIter segs(sched, pair);
+      for (WorkSeg g; !p.stall && segs.next(g);) {
         int mt, nt;
-        tile_coords(t, num_m, num_n, p.group_m, p.group_n, mt, nt);
+        tile_coords(g.tile, num_m, num_n, p.group_m, p.group_n, mt, nt);
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kSiteProducerEmpty)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPairABytes + kBStage));
           const uint32_t bar = map_to_cta(smem_addr(&full[stage]), 0);
@@ -195,11 +193,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int u = pair; u < num_units && ok && num_kb > 0; u += num_pairs, ++it) {
-        const int t = u % num_tiles;
-        const int sidx = u / num_tiles;
-        const int kb0 = static_cast<int>(static_cast<int64_t>(sidx) * num_kb / splits);
-        const int kb1 = static_cast<int>(static_cast<int64_t>(sidx + 1) * num_kb / splits);
+      SegIter segs(sched, pair);
+      for (WorkSeg g; ok && num_kb > 0 && segs.next(g); ++it) {
+        const int kb0 = g.kb0;
+        const int kb1 = g.kb1;
 
         // the MMAs of one K step into one 256-column block of the accumulator
         auto issue = [&](int st, int kbv, int h, uint32_t d_tmem) {
@@ -302,11 +299,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     OutStage os{&tma_c, sOut + (warp - 2) * 2 * kOutBoxBytes, 0u};
     int it = 0;
-    for (int u = pair; u < num_units; u += num_pairs, ++it) {
-      const int t = u % num_tiles;
-      const int sidx = u / num_tiles;
+    SegIter segs(sched, pair);
+    for (WorkSeg g; segs.next(g); ++it) {
       int mt, nt;
-      tile_coords(t, num_m, num_n, p.group_m, p.group_n, mt, nt);
+      tile_coords(g.tile, num_m, num_n, p.group_m, p.group_n, mt, nt);
       const int acc = it % kNumAcc;
       const uint32_t use = static_cast<uint32_t>(it / kNumAcc);
       if (num_kb > 0) {
@@ -320,7 +316,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int h = 0; h < NSUB; ++h) {
         const uint32_t te = map_to_cta(smem_addr(&tempty[NSUB == 1 ? acc : h]), 0);
         epilogue_tile<MODE>(p, tbase + static_cast<uint32_t>(h * kBN), mt * kPairTileM + row_local,
-                            nt * NSUB + h, cstart, rows_valid, num_kb > 0, sidx, splits, os, [&] {
+                            nt * NSUB + h, cstart, rows_valid, num_kb > 0, g.slot, g.slots, os, [&] {
                               tc_fence_before();
                               __syncwarp();
                               if (lane == 0) mbar_arrive_cluster(te);

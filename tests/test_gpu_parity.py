@@ -415,11 +415,15 @@ def test_single_cta_variant_empty_and_single_row(single_cta):
 
 
 def test_variants_agree_bitwise(monkeypatch):
-    # the three kernels accumulate every logit over K in the same order (and
-    # here split dHidden the same way), so their outputs agree bit for bit
+    # the three kernels accumulate every logit over K in the same order, so
+    # with dHidden's K range left whole their outputs agree bit for bit (split,
+    # which tiles form the split tail depends on each variant's tile count;
+    # each variant's split dHidden is checked against the oracle by the
+    # parity suite)
     w = synth.workload("tiny", seed=21, N=900, H=320, V=3000)
     inp = synth.make_inputs(w, device=DEV)
     res = []
+    monkeypatch.setenv("LMHEAD_DH_SPLIT", "1")
     for variant in ("pair", "single", "wide"):
         monkeypatch.setenv("LMHEAD_GEMM", variant)  # the previous value comes back after the test
         sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=256)
@@ -431,6 +435,48 @@ def test_variants_agree_bitwise(monkeypatch):
     for other in res[1:]:
         for a, b in zip(res[0], other):
             assert torch.equal(a, b)
+
+
+_TAIL_ORACLE = {}
+
+
+@pytest.mark.parametrize("variant", ["pair", "single", "wide"])
+@pytest.mark.parametrize("share", ["2", "3", "4"])
+def test_dhidden_tail_tiles_split_into_up_to_four_parts(monkeypatch, variant, share):
+    # 2560 kept rows in one chunk, H = 2048, V = 8000 (125 K blocks): on 76
+    # CTA pairs the 80 pair tiles run one whole wave and a tail of 4 tiles
+    # cut into K parts, the 160 one-CTA tiles on 152 CTAs likewise (8 tail
+    # tiles), and the 40 wide tiles form a tail alone (in two rounds of parts
+    # with 3 or 4 parts allowed); the whole dhidden -- rows written directly
+    # and rows summed from partials -- against the oracle
+    monkeypatch.setenv("LMHEAD_GEMM", variant)
+    monkeypatch.setenv("LMHEAD_DH_SPLIT", share)
+    w = synth.workload("tiny", seed=41, N=2560, H=2048, V=8000)
+    inp = synth.make_inputs(w, device=DEV)
+    keep = torch.ones(w.N, dtype=torch.uint8, device=DEV)
+    sc = LMHeadScorer(w.N, w.H, w.V, chunk_rows=2560)
+    lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep)
+    dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                         inp["grad_logprob"], inp["grad_entropy"])
+    dh2, _ = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
+                         inp["grad_logprob"], inp["grad_entropy"])
+    torch.cuda.synchronize()
+    assert sc.status() == 0
+    assert torch.equal(dh, dh2)  # the partial sums are added in a fixed order
+    if "ref" not in _TAIL_ORACLE:
+        h, W = to64(inp["hidden"]), to64(inp["weight"])
+        y = inp["targets"].cpu().numpy()
+        _TAIL_ORACLE["ref"] = O.backward(h, W, y, np.ones(w.N, np.uint8),
+                                            inp["grad_logprob"].cpu().double().numpy(),
+                                            inp["grad_entropy"].cpu().double().numpy())
+    odh, odW = _TAIL_ORACLE["ref"]
+    assert_frob_close(to64(dh), odh, "dhidden")
+    assert_frob_close(dW.cpu().double().numpy(), odW, "dW")
+    # every row on its own as well: a tile whose partial sums were dropped or
+    # added twice shows up in its rows even when the whole matrix passes
+    got = to64(dh)
+    rel = np.linalg.norm(got - odh, axis=1) / np.linalg.norm(odh, axis=1)
+    assert rel.max() < 2e-2, rel.max()
 
 
 @pytest.mark.parametrize("nk", [255, 256, 257, 511, 513, 1000])

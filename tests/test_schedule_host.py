@@ -1,12 +1,13 @@
 """Host checks of the persistent GEMMs' work schedule, no GPU needed.
 
 ``tests/host/schedule_check.cu`` includes the kernels' own scheduling helpers
-(tile raster, chunk spans, dHidden K-split rule) and runs them on the CPU:
-every tile index must map to a distinct tile of the grid, the chunks must
-cover the kept rows in order, the split count must stay within bounds, and
-the 512-column tiles of the CTA-pair kernel (row tile x two 256-column
-blocks x K part) must cover every tile and K block once, counted as the
-dHidden reduction counts them.
+(tile raster, chunk spans, the plain / split-tail work schedule) and runs them
+on the CPU: every tile index must map to a distinct tile of the grid, the
+chunks must cover the kept rows in order, every worker's segments together
+must cover every (tile, K block) once, the split tail in at most max_split
+parts per tile (slots in K order, faster than unsplit), and the
+512-column tiles of the CTA-pair kernel must cover every 256-column tile once,
+counted and ordered as the dHidden reduction counts and orders them.
 """
 
 import os
