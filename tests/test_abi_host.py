@@ -61,7 +61,7 @@ def test_workspace_size_formula(L):
     assert b - a < 65536 * 64
     assert a < 65536 * V * 2 / 4  # far below a bf16 [N, V] logit buffer
     # chunk buffers: dz [C, V] bf16 + h_c [C, H] bf16 + partials [V/256, C] x 16 B
-    # + dHidden K-split partials [4, C, H] fp32
+    # + dHidden tail partials [4, C, H] fp32
     C = 8192
     core = C * V * 2 + C * H * 2 + (V // 256 + 1) * C * 16 + 4 * C * H * 4
     assert core <= a <= core + 65536 * 48 + 4096
