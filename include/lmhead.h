@@ -64,10 +64,11 @@
  *     LMHEAD_DH_SPLIT = 1 .. 4 caps the K parts of the dHidden tiles of a
  *     partly filled last wave (default 4; 1 never splits K).  The variants
  *     accumulate in the same order and differ at most by which dHidden tiles
- *     are split (the tile count differs by variant).  LMHEAD_FAULT = "tensor_map", "launch" or "stall" makes the
- *     next calls fail on purpose for tests: a tensor-map encode or a launch
- *     reports LMHEAD_ECUDA, or the GEMM producers issue no loads so that the
- *     bounded pipeline waits run out (LMHEAD_ETIMEOUT).
+ *     are split (the tile count differs by variant).  LMHEAD_FAULT =
+ *     "tensor_map", "launch" or "stall" makes the next calls fail on purpose
+ *     for tests: a tensor-map encode or a launch reports LMHEAD_ECUDA, or the
+ *     GEMM producers issue no loads so that the bounded pipeline waits run
+ *     out (LMHEAD_ETIMEOUT).
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H
