@@ -217,11 +217,14 @@ __global__ void gather_vec_kernel(const int32_t* __restrict__ idx, const int32_t
 // Split-V merge of the per-tile (m, s, u, t) partials of one chunk:
 //   M = max m_i, S = sum s_i e^(m_i - M), U = sum e^(m_i - M)(u_i + s_i (m_i - M))
 //   lse = M + log S, logprob = t - lse, entropy = log S - U / S.
-// kMergeLanes threads per row, each taking every kMergeLanes-th vocab tile with
-// a running max-shifted (M, S, U); the lanes of a row are combined with
-// shuffles.  Two rows per warp: each load instruction of a warp touches 16
-// vocab tiles x 2 consecutive rows = 16 full 32-byte sectors.
-constexpr int kMergeLanes = 16;
+// A block takes kMergeRows consecutive rows; its 256 threads form 32 groups
+// of one thread per row, group j taking the vocab tiles j, j + 32, ... with
+// a running max-shifted (M, S, U), so each load instruction of a warp reads 4
+// vocab tiles x 8 consecutive rows: four whole 128-byte lines.  The 32
+// partial reductions of a row are combined in a fixed order: the 4 groups of
+// a warp by shuffles, then the 8 warps through shared memory.
+constexpr int kMergeRows = 8;
+constexpr int kMergeGroups = 256 / kMergeRows;
 
 __device__ __forceinline__ void merge_pair(float& M, float& S, float& U, float m2, float s2,
                                            float u2) {
@@ -237,44 +240,51 @@ __device__ __forceinline__ void merge_pair(float& M, float& S, float& U, float m
   M = N;
 }
 
-__global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const int32_t* d_nk,
-                             int chunk_index, int chunk_rows, int want_entropy,
-                             float* __restrict__ lp_c, float* __restrict__ ent_c,
-                             float* __restrict__ lse_c, float4* __restrict__ raw_c) {
+__global__ void __launch_bounds__(256) merge_kernel(const float4* __restrict__ part, int num_vt,
+                                                    const int32_t* d_nk, int chunk_index,
+                                                    int chunk_rows, int want_entropy,
+                                                    float* __restrict__ lp_c,
+                                                    float* __restrict__ ent_c,
+                                                    float* __restrict__ lse_c,
+                                                    float4* __restrict__ raw_c) {
   int chunk_start, rows;
   chunk_span(*d_nk, chunk_rows, chunk_index, chunk_start, rows);
-  if (static_cast<int>((blockIdx.x * blockDim.x) / kMergeLanes) >= rows) return;  // whole block
-  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r0 = static_cast<int>(blockIdx.x) * kMergeRows;
+  if (r0 >= rows) return;  // whole block
+  const int ri = threadIdx.x & (kMergeRows - 1);
+  const int grp = threadIdx.x / kMergeRows;
   const int lane = threadIdx.x & 31;
-  const int sub = lane & (kMergeLanes - 1);
-  const int r = (g >> 5) * (32 / kMergeLanes) + (lane / kMergeLanes);
+  const int warp = threadIdx.x >> 5;
+  const int r = r0 + ri;
   float M = -INFINITY, S = 0.f, U = 0.f, T = -INFINITY;
   if (r < rows) {
-    int v = sub;
-    for (; v + 3 * kMergeLanes < num_vt; v += 4 * kMergeLanes) {
+    int v = grp;
+    for (; v + 3 * kMergeGroups < num_vt; v += 4 * kMergeGroups) {
       float4 q[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) q[k] = part[static_cast<int64_t>(v + k * kMergeLanes) * chunk_rows + r];
+      for (int k = 0; k < 4; ++k)
+        q[k] = part[static_cast<int64_t>(v + k * kMergeGroups) * chunk_rows + r];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         merge_pair(M, S, U, q[k].x, q[k].y, q[k].z);
         T = fmaxf(T, q[k].w);
       }
     }
-    for (; v < num_vt; v += kMergeLanes) {
+    for (; v < num_vt; v += kMergeGroups) {
       const float4 q = part[static_cast<int64_t>(v) * chunk_rows + r];
       merge_pair(M, S, U, q.x, q.y, q.z);
       T = fmaxf(T, q.w);
     }
   }
+  // the 4 groups of this warp: lanes ri, ri + 8, ri + 16, ri + 24
 #pragma unroll
-  for (int off = 1; off < kMergeLanes; off <<= 1) {
+  for (int off = kMergeRows; off < 32; off <<= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
     const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
     const float u2 = __shfl_xor_sync(0xffffffffu, U, off);
     const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
     // the lower lane's value first, so both lanes of a pair hold the same sum
-    if ((sub & off) == 0) {
+    if ((lane & off) == 0) {
       merge_pair(M, S, U, m2, s2, u2);
     } else {
       float m1 = m2, s1 = s2, u1 = u2;
@@ -283,7 +293,18 @@ __global__ void merge_kernel(const float4* __restrict__ part, int num_vt, const 
     }
     T = fmaxf(T, t2);
   }
-  if (sub != 0 || r >= rows) return;
+  __shared__ float4 warp_part[256 / 32][kMergeRows];
+  if (lane < kMergeRows) warp_part[warp][lane] = make_float4(M, S, U, T);
+  __syncthreads();
+  if (threadIdx.x >= kMergeRows || r >= rows) return;
+  // thread ri (warp 0, lane ri) adds the warps' reductions of its row in order
+  M = -INFINITY; S = 0.f; U = 0.f; T = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 256 / 32; ++w) {
+    const float4 q = warp_part[w][ri];
+    merge_pair(M, S, U, q.x, q.y, q.z);
+    T = fmaxf(T, q.w);
+  }
   if (raw_c != nullptr) {  // a vocabulary shard: keep the unnormalised reduction
     raw_c[chunk_start + r] = make_float4(M, S, U, T);
     return;
@@ -494,10 +515,8 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* hidden, const int32_t* idx,
 cudaError_t launch_merge(const float4* part, int num_vt, const int32_t* d_nk, int chunk_index,
                          int chunk_rows, int want_entropy, float* lp_c, float* ent_c,
                          float* lse_c, float4* raw_c, cudaStream_t s) {
-  merge_kernel<<<blocks_for(static_cast<int64_t>(chunk_rows) * kMergeLanes, 256), 256, 0, s>>>(
-      part, num_vt, d_nk, chunk_index,
-                                                           chunk_rows, want_entropy, lp_c, ent_c,
-                                                           lse_c, raw_c);
+  merge_kernel<<<blocks_for(chunk_rows, kMergeRows), 256, 0, s>>>(
+      part, num_vt, d_nk, chunk_index, chunk_rows, want_entropy, lp_c, ent_c, lse_c, raw_c);
   return cudaGetLastError();
 }
 
