@@ -131,3 +131,31 @@ def test_changing_batch_size_reuses_one_workspace():
     assert len(keys) == 1
     # grew only for the two sizes larger than every earlier one
     assert len(set(sizes)) <= 2
+
+
+def test_backward_saves_no_full_vocabulary_activation():
+    # twinkle pull request #283, section 1: the backward must not keep a
+    # full-vocabulary activation alive.  Every tensor the op saves is either
+    # one of its inputs (no new memory) or a per-row vector (lse, entropy):
+    # the extra bytes grow with the rows, never with rows x vocabulary.
+    extra = {}
+    for N in (512, 1024):
+        w, inp = _inputs(seed=310, N=N, H=128, V=20000)
+        h, W = _leaves(inp)
+        inputs = {t.data_ptr() for t in (h, W, inp["targets"], inp["keep"])}
+        saved = []
+
+        def pack(t):
+            saved.append((t.data_ptr(), tuple(t.shape), t.numel() * t.element_size()))
+            return t
+
+        with torch.autograd.graph.saved_tensors_hooks(pack, lambda t: t):
+            lp, ent = hidden_to_logprobs(h, W, inp["targets"], inp["keep"],
+                                         return_entropy=True, entropy_requires_grad=True)
+        (lp.sum() + ent.sum()).backward()
+        torch.cuda.synchronize()
+        assert h.grad is not None and W.grad is not None
+        new = [(shape, b) for ptr, shape, b in saved if ptr not in inputs]
+        assert all(w.V not in shape for shape, _ in new), new
+        extra[N] = sum(b for _, b in new)
+    assert extra[512] == 512 * 8 and extra[1024] == 1024 * 8  # lse + entropy, fp32
