@@ -6,6 +6,7 @@ Frobenius error (bf16 inputs, fp32 accumulation, bf16 logit gradient).
 """
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -39,9 +40,15 @@ def _run_both(w, chunk_rows=0, want_entropy=True, grad_entropy=True, keep_overri
     g_ent = inp["grad_entropy"] if grad_entropy else None
     lp, ent, lse = sc.forward(inp["hidden"], inp["weight"], inp["targets"], keep, want_entropy)
     out = dict(lp=lp, ent=ent, lse=lse)
+    dW0 = None
     if check_bwd:
+        # with accumulation the gradient is added to a seeded prior one
+        if accumulate:
+            g = torch.Generator(device=DEV).manual_seed(w.seed)
+            dW0 = torch.randn(w.V, w.H, generator=g, device=DEV)
         dh, dW = sc.backward(inp["hidden"], inp["weight"], inp["targets"], keep, lse, ent,
-                             inp["grad_logprob"], g_ent, accumulate=accumulate)
+                             inp["grad_logprob"], g_ent,
+                             dweight=None if dW0 is None else dW0.clone(), accumulate=accumulate)
         out.update(dh=dh, dW=dW)
     torch.cuda.synchronize()
     assert sc.status() == 0
@@ -58,6 +65,8 @@ def _run_both(w, chunk_rows=0, want_entropy=True, grad_entropy=True, keep_overri
     if check_bwd:
         odh, odW = O.backward(h, W, y, keep_np, inp["grad_logprob"].cpu().double().numpy(),
                               None if g_ent is None else g_ent.cpu().double().numpy())
+        if dW0 is not None:
+            odW = odW + dW0.cpu().double().numpy()
         assert_frob_close(to64(out["dh"]), odh, "dhidden")
         assert_frob_close(out["dW"].cpu().double().numpy(), odW, "dW")
         assert (out["dh"].cpu()[torch.from_numpy(skipped)] == 0).all()
@@ -603,6 +612,40 @@ def test_random_shape_sweep(monkeypatch):
         monkeypatch.setenv("LMHEAD_GEMM", variant)  # restored after the test
         w = synth.workload("tiny", seed=300 + case, N=N, H=H, V=V)
         _run_both(w, chunk_rows=chunk, keep_override=keep, blocksparse=bs, grad_entropy=ent)
+
+
+def test_random_sweep_of_schedules_and_accumulation(monkeypatch):
+    # seeded random problems up to 6000 rows and 2048 columns, over the
+    # dHidden split caps (whole tiles, tails in 2-4 K parts, as the tile count
+    # and fill fall), the GEMM variants and the default per-contraction
+    # choice, both strategies, entropy gradient on or off and dW accumulated
+    # onto a prior gradient or written; every one must match the oracle
+    if os.environ.get("LMHEAD_GEMM"):
+        pytest.skip("picks the GEMM variant of every case itself")
+    rng = np.random.default_rng(7)
+    for case in range(30):
+        while True:
+            N = int(rng.integers(1, 6000))
+            H = int(rng.choice([8, 24, 64, 136, 256, 512, 520, 1024, 1536, 2048]))
+            V = int(rng.integers(1, 30000))
+            if N * H * V <= 3e9:
+                break
+        chunk = int(rng.choice([0, 256, 512, 768, 1280, 2048, 4096]))
+        density = float(rng.choice([0.0, 0.02, 0.3, 0.7, 1.0]))
+        keep = (rng.random(N) < density).astype(np.uint8)
+        variant = str(rng.choice(["pair", "single", "wide", "default"]))
+        split = str(rng.choice(["1", "2", "3", "4"]))
+        bs = bool(rng.integers(0, 2))
+        ent = bool(rng.integers(0, 2))
+        acc = bool(rng.integers(0, 2))
+        if variant == "default":
+            monkeypatch.delenv("LMHEAD_GEMM", raising=False)
+        else:
+            monkeypatch.setenv("LMHEAD_GEMM", variant)
+        monkeypatch.setenv("LMHEAD_DH_SPLIT", split)  # both restored after the test
+        w = synth.workload("tiny", seed=1000 + case, N=N, H=H, V=V)
+        _run_both(w, chunk_rows=chunk, keep_override=keep, blocksparse=bs, grad_entropy=ent,
+                  accumulate=acc)
 
 
 @pytest.mark.parametrize("variant", ["pair", "single", "wide"])
