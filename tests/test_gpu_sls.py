@@ -70,6 +70,26 @@ def test_strided_rows_and_metric_only_entropy():
     _run(d, None, grad_entropy=False, want_entropy=False)
 
 
+def test_random_sweep_of_shapes_strides_and_dtypes():
+    # seeded problems: row counts, vocabularies down to one token, bf16 or
+    # fp32 logits, row strides that keep rows 16-byte aligned or not (the
+    # vector and the scalar path), logit scales, keep densities, and the
+    # entropy as a loss term, a metric or absent
+    rng = np.random.default_rng(57)
+    for case in range(12):
+        N = int(rng.integers(1, 600))
+        V = int(rng.integers(1, 20000))
+        dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float32
+        ld = V + int(rng.choice([0, 1, 3, 8, 64]))
+        d = synth.make_logits(N, V, seed=580 + case, std=float(rng.choice([0.5, 2.0, 8.0])),
+                              dtype=dtype, device=DEV, ld=ld)
+        density = float(rng.choice([0.0, 0.3, 1.0, -1.0]))  # -1: no mask
+        keep = None if density < 0 else (rng.random(N) < density).astype(np.uint8)
+        ge = bool(rng.integers(0, 2))
+        want = True if ge else bool(rng.integers(0, 2))
+        _run(d, keep, grad_entropy=ge, want_entropy=want)
+
+
 def test_float32_logits():
     d = synth.make_logits(150, 3001, seed=52, dtype=torch.float32, device=DEV)
     _run(d, None)
