@@ -488,6 +488,24 @@ def test_dhidden_tail_tiles_split_into_up_to_four_parts(monkeypatch, variant, sh
     assert rel.max() < 2e-2, rel.max()
 
 
+def test_wide_tiles_chosen_per_contraction(monkeypatch):
+    # LMHEAD_WIDE names the contractions on 256 x 512 tiles (the rest on
+    # 256 x 256): each choice matches the oracle, and the forward results
+    # agree bit for bit across choices (every variant accumulates a logit
+    # over K in the same order)
+    monkeypatch.delenv("LMHEAD_GEMM", raising=False)  # it would take precedence
+    w = synth.workload("tiny", seed=33, N=1500, H=1024, V=6000)
+    first = None
+    for wide in ("none", "fwd,dz", "dh", "dw,dh", "fwd,dz,dh,dw"):
+        monkeypatch.setenv("LMHEAD_WIDE", wide)  # restored after the test
+        _, _, _, out, _ = _run_both(w, chunk_rows=512)
+        fwd = [out[k].clone() for k in ("lp", "ent", "lse")]
+        if first is None:
+            first = fwd
+        for a, b in zip(first, fwd):
+            assert torch.equal(a, b), wide
+
+
 @pytest.mark.parametrize("nk", [255, 256, 257, 511, 513, 1000])
 def test_chunk_boundaries(nk):
     # the kept rows are cut into equal 256-aligned chunks on the device; Nk
