@@ -313,8 +313,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(run_config(args, w.N, w.H, w.V, nk, world, ent_grad),
-                       sample_rows_per_step=rows),
+        # the GPU arm's config exactly; the sample size is a key of its own
+        "config": run_config(args, w.N, w.H, w.V, nk, world, ent_grad),
+        "sample_rows_per_step": rows,
         "tflops": flops / tot / 1e12,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _oracle_cores(), "kind": "oracle",
                          "sample": f"{rows} kept rows per step, full H and V, forward"
