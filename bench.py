@@ -164,7 +164,7 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in getattr(self, "lines", []):
             parts = [p.strip() for p in ln.split(",")]
@@ -175,11 +175,16 @@ class ClockSampler:
                 mx = float(parts[2])
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": statistics.median(power) if power else None}
 
 
 def _oracle_sample(inp, keep, rows, want_grad=True):
@@ -533,6 +538,15 @@ def run_ours(args):
             "clocks": clk.summary(), "device_status": status_timed, "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        # under the power limit the step time is energy / power: the median
+        # board power over the timed region times the step time (this GPU).
+        # The board's power reading trails the load by a fraction of a
+        # second, so it is used only over timed regions of 1.5 s or more.
+        pw = line["clocks"]["power_w"]
+        if pw is not None and world == 1 and sec >= 1.5 and line["clocks"]["samples"] >= 10:
+            j = pw * ms_max / args.steps / 1e3
+            line["energy"] = {"board_w_median": pw, "j_per_step": j,
+                              "pj_per_flop": j / flops_step * 1e12 if flops_step else None}
         rec = recorded_traffic(roof["kernel"], line["config"])
         if rec is not None:
             roof["traffic"] = rec["dram_bytes_per_launch"]
