@@ -51,3 +51,24 @@ def test_reference_arm_prints_the_contract_line():
     cfg = line["config"]
     assert cfg == bench.run_config(args, cfg["N"], cfg["H"], cfg["V"], cfg["kept_rows"], 1, True)
     assert line["sample_rows_per_step"] == min(32, cfg["kept_rows"])  # --ref-rows default
+
+
+def test_clock_summary_reads_clocks_reasons_and_power():
+    # nvidia-smi csv lines: index, clocks.sm, clocks.max.sm, power.draw, the
+    # active reasons bitmask, then hw_slowdown, hw_thermal_slowdown,
+    # sw_thermal_slowdown and sw_power_cap as Active / Not Active
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "0, 1500, 2070, 1350.5, 0x4, Not Active, Not Active, Not Active, Active\n",
+        "0, 1540, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active\n",
+        "0, 1520, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active\n",
+        "garbage\n",
+    ]
+    got = s.summary()
+    assert got["sm_mhz"] == 1520 and got["sm_max_mhz"] == 2070 and got["samples"] == 3
+    assert got["reasons"] == ["sw_power_cap"]
+    assert got["power_w"] == (1350.5 + 1390.0) / 2  # the unreadable power sample is skipped
+    empty = bench.ClockSampler(0)
+    empty.lines = []
+    assert empty.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                               "samples": 0, "power_w": None}
