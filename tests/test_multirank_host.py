@@ -5,7 +5,8 @@ all-reduce of the weight gradient after the backward (the library's
 allreduce_weight_grad, run here on CPU tensors with the oracle's per-rank
 gradients), and bench.py reduces the timing (max over ranks) and the
 kept-row count (sum over ranks).  How bench.py treats --gpus is checked
-without starting ranks.
+without starting ranks, and the reference arm (CPU only) runs under two
+launcher ranks.
 """
 
 import os
@@ -182,3 +183,23 @@ def test_data_parallel_ranks_share_the_weight_and_not_the_batch():
                               "cpu", weight_seed=base.seed)
     assert torch.equal(r1["hidden"], again["hidden"]) and torch.equal(r1["weight"],
                                                                       again["weight"])
+
+
+def test_reference_arm_under_two_launcher_ranks_prints_one_line():
+    # launched as the driver launches N = 2 (torch.distributed.run, 127.0.0.1):
+    # rank 0 alone times the oracle and prints the line; the other rank exits 0
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}",
+           os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--workload", "tiny", "--steps", "1", "--warmup", "1"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, capture_output=True, text=True, cwd=root, timeout=600, env=env)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
